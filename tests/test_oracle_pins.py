@@ -1,0 +1,54 @@
+"""The oracle against its pins, and planted mistakes against the pins.
+
+Every pin is described in oracle_pins.py.  The second test copies the oracle's
+C source, plants one plausible mistake (a wrong index, a dropped term, a sign,
+a transposed operand), builds the copy and checks that at least one pin fails.
+"""
+import pytest
+
+import oracle
+from oracle_pins import ALL_CHECKS
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check):
+    check(oracle.load())
+
+
+MUTATIONS = [
+    ("slot_off_by_one", "return blk * block_size + pos % block_size;",
+     "return blk * block_size + pos % block_size + 1;"),
+    ("head_map_modulo", "int h = g / G;", "int h = g % J->hkv;"),
+    ("in_block_offset", "int64_t off = t % J->bs;", "int64_t off = (t + 1) % J->bs;"),
+    ("table_index", "+ t / J->bs];", "+ t % J->bs];"),
+    ("score_sign", "x[t] = J->scale * acc;", "x[t] = -J->scale * acc;"),
+    ("no_max_subtraction", "x[t] = exp(x[t] - mx);", "x[t] = exp(x[t]);"),
+    ("no_normalisation", "double w = x[t] / sum;", "double w = x[t];"),
+    ("last_token_dropped", "for (int t = 0; t < n; ++t) {\n            double w",
+     "for (int t = 0; t + 1 < n; ++t) {\n            double w"),
+    ("keys_as_values", "o[d] += w * V[", "o[d] += w * K["),
+    ("q_row_of_kv_head", "qd[d] = orc_load(J->q, (size_t)r * D + d, J->dtype);",
+     "qd[d] = orc_load(J->q, ((size_t)s * J->hq + h) * D + d, J->dtype);"),
+    ("append_transposed_layout",
+     "size_t dst = (size_t)(((blk * num_kv_heads + h) * block_size + off)) * row;",
+     "size_t dst = (size_t)(((blk * block_size + off) * num_kv_heads + h)) * row;"),
+    ("half_subnormal_exponent", "v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -25);"),
+    ("bf16_shift", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    with open(oracle.SOURCE) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib = oracle.load(oracle.build(str(path), str(tmp_path / "libmutant.so"), force=True))
+    caught = []
+    for check in ALL_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, ValueError) as exc:  # a mutant may also fail its own checks
+            caught.append((check.__name__, type(exc).__name__))
+    assert caught, f"planted mistake {name} passed every pin"
