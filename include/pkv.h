@@ -1,0 +1,253 @@
+/*
+ * pkv.h -- C ABI of a paged KV cache and single-query (decode) attention over
+ * it, for one GPU (sm_103a).
+ *
+ * The operations follow "vLLM Architecture and Installation", Example 3
+ * (paged KV cache block tables) and "Batching and Scheduling", Example 1
+ * (utilization of a single decoding request):
+ *   - the cache is a pool of fixed-size blocks; each sequence owns a block
+ *     table listing its physical blocks in logical order;
+ *   - each step appends every running sequence's newest K/V row to the slot
+ *     table[pos / block_size] * block_size + pos % block_size;
+ *   - each sequence's single query token then attends over all of its cached
+ *     tokens, read through its block table.
+ *
+ * Conventions for every call:
+ *   - Tensor arguments are plain pointers.  "device" pointers must be
+ *     addresses in the memory of the selected GPU; "host" pointers are
+ *     ordinary CPU memory.  The caller owns every buffer it passes; the
+ *     library frees only memory it allocated itself (kv_pool_create with a
+ *     NULL buffer).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Device work is enqueued asynchronously on it; device pointers
+ *     must stay valid until that work completes.
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     failed validation returns a status code and launches nothing; no call
+ *     throws or aborts.  kv_last_error() describes the last failure of the
+ *     calling thread.
+ *   - Errors that only the device can see (a block id outside the pool, a
+ *     slot outside the pool, a context longer than its table) set a bit in a
+ *     per-device status word and the offending item is skipped or clamped;
+ *     kv_device_status() reports and clears it.
+ *   - Calls are thread-safe as long as two threads do not write the same
+ *     buffers at the same time.
+ *
+ * Pool layout in device memory (one pool serves every layer; a block id
+ * addresses the same block in every layer):
+ *   layer l, K: [num_blocks][num_kv_heads][block_size][head_dim]
+ *   layer l, V: same shape, right after layer l's K
+ *   so one (block, kv_head) tile of K is block_size*head_dim contiguous
+ *   elements.  Block tables are int32 [num_seqs][max_blocks_per_seq], row
+ *   major, entries past the sequence's last block are ignored (-1 by
+ *   convention).  context_lens[s] counts every cached token of sequence s,
+ *   including the one appended in the current step.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Every declaration below is exported from the shared library, which is
+ * otherwise built with hidden symbol visibility. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype_t;
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,         /* a pointer, size or shape is not acceptable */
+    KV_ERR_UNSUPPORTED = 2,         /* valid, but not a shape/dtype the kernels cover */
+    KV_ERR_OUT_OF_MEMORY = 3,       /* a library allocation failed */
+    KV_ERR_OUT_OF_BLOCKS = 4,       /* host allocator: not enough free blocks */
+    KV_ERR_WORKSPACE_TOO_SMALL = 5, /* see paged_decode_workspace_bytes */
+    KV_ERR_CUDA = 6,                /* a CUDA runtime call failed */
+    KV_ERR_DEVICE_CHECK = 7,        /* the device flagged a bad block id / slot / length */
+    KV_ERR_DEVICE_TIMEOUT = 8,      /* a bounded wait inside a kernel ran out */
+    KV_ERR_NOT_FOUND = 9            /* host allocator: unknown sequence id */
+} kv_status_t;
+
+/* Bits of the per-device status word (kv_device_status). */
+#define KV_FLAG_BAD_BLOCK_ID   0x1u /* a table entry outside [0, num_blocks) was read */
+#define KV_FLAG_BAD_SLOT       0x2u /* an append slot >= num_blocks*block_size */
+#define KV_FLAG_BAD_CONTEXT    0x4u /* context_lens[s] < 0 or > max_blocks_per_seq*block_size */
+#define KV_FLAG_TIMEOUT        0x8u /* a kernel gave up a bounded wait */
+
+/* Human-readable name of a status code (static string). */
+const char* kv_status_string(kv_status_t status);
+
+/* Description of the last failed call on this thread ("" if none). */
+const char* kv_last_error(void);
+
+/* ------------------------------------------------------------------ pool */
+
+typedef struct {
+    int num_layers;
+    int num_blocks;   /* physical blocks; a block holds block_size tokens */
+    int block_size;   /* tokens per block (1..1024) */
+    int num_kv_heads;
+    int head_dim;     /* head_dim * element size must be a multiple of 16 bytes */
+    kv_dtype_t dtype;
+    int device;       /* CUDA device ordinal */
+} kv_pool_config_t;
+
+typedef struct kv_pool kv_pool_t;
+
+/* Bytes of a pool: 2 (K and V) * num_layers * num_blocks * block_size *
+ * num_kv_heads * head_dim * element size ("vLLM Architecture and
+ * Installation", Example 6: 16 x 8 x (128 + 128) x 2 = 65,536 bytes per layer
+ * per block).  Returns 0 for an invalid configuration. */
+size_t kv_pool_bytes(const kv_pool_config_t* cfg);
+
+/* Create a pool.  device_buffer: a device buffer of at least kv_pool_bytes()
+ * bytes, 256-byte aligned, owned by the caller and adopted (not copied, not
+ * freed); or NULL, in which case the library allocates (and later frees) the
+ * memory with cudaMalloc.  The contents are not initialised. */
+kv_status_t kv_pool_create(const kv_pool_config_t* cfg, void* device_buffer, size_t buffer_bytes,
+                           kv_pool_t** pool_out);
+
+/* Destroy a pool (frees only memory the library allocated).  NULL is a no-op. */
+void kv_pool_destroy(kv_pool_t* pool);
+
+/* Device addresses of layer `layer`'s K and V caches. */
+kv_status_t kv_pool_layer(const kv_pool_t* pool, int layer, void** k_cache, void** v_cache);
+
+/* Copy of the pool's configuration. */
+kv_status_t kv_pool_config(const kv_pool_t* pool, kv_pool_config_t* cfg_out);
+
+/* ---------------------------------------------------------------- append */
+
+/* Slot of every sequence's newest token (position context_lens[s] - 1):
+ *   slot_mapping[s] = table[s][p / block_size] * block_size + p % block_size,
+ * or -1 where context_lens[s] <= 0 ("vLLM Architecture and Installation",
+ * Example 3).  All pointers are device pointers: block_tables
+ * int32[num_seqs][max_blocks_per_seq], context_lens int32[num_seqs],
+ * slot_mapping int32[num_seqs] (written).  A table entry outside
+ * [0, num_blocks) gives slot -1 and sets KV_FLAG_BAD_BLOCK_ID; a length past
+ * the table gives -1 and sets KV_FLAG_BAD_CONTEXT. */
+kv_status_t kv_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int block_size,
+                            int num_blocks, int32_t* slot_mapping, void* stream);
+
+/* Write each token's K and V rows into layer `layer` of the pool at its slot
+ * ("vLLM Architecture and Installation", Example 3: the slot mapping tells the
+ * attention kernel where new keys and values go).  Bit-exact copy, no dtype
+ * conversion (k and v have the pool's dtype).
+ *   k, v          device [n_tokens][num_kv_heads][head_dim]
+ *   slot_mapping  device int32[n_tokens]; a negative slot writes nothing;
+ *                 a slot >= num_blocks*block_size writes nothing and sets
+ *                 KV_FLAG_BAD_SLOT
+ *   seq_ids       device int32[n_tokens] or NULL; not used for addressing,
+ *                 a token whose seq_id is negative is padding and writes
+ *                 nothing
+ * Two tokens of one call must not share a slot (the result would be either
+ * row). n_tokens == 0 is a no-op. */
+kv_status_t kv_append(kv_pool_t* pool, int layer, const int32_t* seq_ids, int n_tokens,
+                      const void* k, const void* v, const int32_t* slot_mapping, void* stream);
+
+/* ------------------------------------------------------- decode attention */
+
+typedef enum {
+    KV_KERNEL_AUTO = 0, /* tensor-core kernel for f16/bf16, FFMA for f32 */
+    KV_KERNEL_FFMA = 1, /* CUDA-core fp32 FMA kernel, any dtype */
+    KV_KERNEL_MMA = 2   /* warp-level tensor-core kernel, f16/bf16 only */
+} kv_kernel_t;
+
+typedef struct {
+    int num_ctas;       /* persistent grid size; 0 = SM count x ctas_per_sm */
+    int ctas_per_sm;    /* 0 = 1 */
+    int consumer_warps; /* compute warps per CTA, 1..15; 0 = 8 */
+    kv_kernel_t kernel;
+    int test_stall;     /* testing only, 0 in normal use: when non-zero, the
+                           producer of CTA 0 stops after one tile so that a
+                           consumer's bounded wait (about 2 s) runs out; the
+                           call then reports KV_ERR_DEVICE_TIMEOUT through
+                           kv_device_status and the output is undefined */
+} kv_decode_options_t;
+
+/* Workspace bytes paged_decode_attention needs for these sizes on `device`
+ * with these options (NULL = defaults). */
+kv_status_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int device,
+                                         const kv_decode_options_t* opts, size_t* bytes_out);
+
+/* Single-query attention over the paged cache, for every sequence s and query
+ * head g (KV head h = g / (num_q_heads / num_kv_heads)):
+ *   out[s][g] = sum_t softmax_t(scale * q[s][g] . K_s[t]) * V_s[t],
+ *   t = 0 .. context_lens[s]-1, K_s[t] = k_cache[table[s][t / bs]][h][t % bs]
+ * ("vLLM Architecture and Installation", Example 3; "Batching and
+ * Scheduling", Example 1).  A sequence with context 0 gets a zero row.
+ *   q            device [num_seqs][num_q_heads][head_dim], dtype
+ *   k_cache,
+ *   v_cache      device, one layer of a pool: [num_blocks][num_kv_heads]
+ *                [block_size][head_dim], dtype; 16-byte aligned
+ *   block_tables device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens device int32 [num_seqs]
+ *   out          device [num_seqs][num_q_heads][head_dim], out_dtype
+ *                (KV_F32, or the same dtype as q)
+ *   workspace    device scratch of workspace_bytes >= the size given by
+ *                paged_decode_workspace_bytes for the same sizes and options;
+ *                no initialisation needed; not to be shared by two calls in
+ *                flight at once
+ * Supported: head_dim 64 or 128, block_size 8..256 a multiple of 8,
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}; dtype f32, f16 or bf16.
+ * The work of all sequences is split evenly over a persistent grid; each CTA
+ * writes an fp32 partial (unnormalised output, running max, running sum) for
+ * every sequence/KV head it only partly covers, and a second kernel merges
+ * the partials (log-sum-exp).  Accumulation is fp32 throughout. */
+kv_status_t paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                   int num_blocks, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, kv_dtype_t dtype, float scale, void* out,
+                                   kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                                   const kv_decode_options_t* opts, void* stream);
+
+/* Synchronise `stream`, then read and clear the status word of `device`.
+ * flags_out (may be NULL) receives the KV_FLAG_* bits.  Returns KV_OK when no
+ * bit was set, KV_ERR_DEVICE_TIMEOUT if the timeout bit was set, else
+ * KV_ERR_DEVICE_CHECK. */
+kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out);
+
+/* --------------------------------------------------- host block allocator */
+
+/* A host-side allocator of physical blocks, the bookkeeping that produces the
+ * block tables ("vLLM Architecture and Installation", Example 3): a FIFO free
+ * queue (initially blocks in increasing order, block 0 held back as the null
+ * block when reserve_null_block is set); extending a sequence takes whole
+ * blocks from the front of the queue, only when a token crosses a block
+ * boundary; releasing a sequence returns its blocks, in table order, to the
+ * back of the queue.  An extension that needs more blocks than are free fails
+ * with KV_ERR_OUT_OF_BLOCKS and changes nothing. */
+typedef struct kv_block_allocator kv_block_allocator_t;
+
+kv_status_t kv_allocator_create(int num_blocks, int block_size, int reserve_null_block,
+                                kv_block_allocator_t** out);
+void kv_allocator_destroy(kv_block_allocator_t* a);
+kv_status_t kv_allocator_extend(kv_block_allocator_t* a, int64_t seq_id, int new_tokens);
+kv_status_t kv_allocator_release(kv_block_allocator_t* a, int64_t seq_id);
+/* table_out (host, capacity entries) receives the sequence's blocks;
+ * num_blocks_out / num_tokens_out may be NULL. */
+kv_status_t kv_allocator_table(const kv_block_allocator_t* a, int64_t seq_id, int32_t* table_out,
+                               int capacity, int* num_blocks_out, int* num_tokens_out);
+kv_status_t kv_allocator_slot(const kv_block_allocator_t* a, int64_t seq_id, int position,
+                              int32_t* slot_out);
+/* The free queue, front first. */
+kv_status_t kv_allocator_free_queue(const kv_block_allocator_t* a, int32_t* out, int capacity,
+                                    int* count_out);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

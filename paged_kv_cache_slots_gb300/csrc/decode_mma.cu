@@ -1,0 +1,247 @@
+// Warp-level tensor-core consumer of the split-context decode kernel
+// (f16/bf16 K/V, head_dim 64 or 128, block_size a multiple of 16, up to 8
+// query heads per KV head).
+//
+// Per 16-token slice of a tile:
+//   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]      (mma m16n8k16, fp32 acc)
+//   online softmax per head on the fp32 scores (base-2 units)
+//   O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T[16 x 8]
+// Tokens are the M dimension, so one tile of K feeds the MMA A operand
+// straight from shared memory (ldmatrix), the G <= 8 heads of the group are
+// the N dimension (padded to 8) and q stays in registers as B fragments.
+// P^T is formed from the score accumulators with movmatrix (transpose in
+// registers) and split into a high and a low half-precision part, so the
+// probabilities carry ~16 significant bits into the PV product.
+// K and V tiles arrive through 2-D tensor maps with a 128-byte swizzle, which
+// makes the eight 16-byte rows of every ldmatrix fall in distinct banks.
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <int DT>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (DT == kBF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// Pack two fp32 values (lower column first) and the residual of the rounding.
+template <int DT>
+__device__ __forceinline__ void pack_split(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    if constexpr (DT == kBF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+        const __nv_bfloat162 l =
+            __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+    } else {
+        const __half2 h = __floats2half2_rn(x0, x1);
+        const __half2 l = __floats2half2_rn(x0 - __low2float(h), x1 - __high2float(h));
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+    }
+}
+
+template <int DT, int D>
+struct MmaPolicy {
+    static constexpr bool kTensor = true;
+    static constexpr bool kScratch = false;
+    static constexpr int KS = D / 16;  // k-steps of QK, m-tiles of PV
+    using T = typename Elem<DT>::T;
+
+    struct State {
+        uint32_t qb[KS][2];  // B fragments of Q^T: head lane/4, dims 16ks + 2(lane%4) (+8)
+        float o[KS][4];      // O^T accumulators: dims 16mi + lane/4 (+8), heads 2(lane%4) (+1)
+        float m[2];          // running max of heads 2(lane%4), 2(lane%4)+1
+        float l[2];          // this lane's share of the running sum
+    };
+
+    __device__ __forceinline__ void begin(State& st, const DecodeArgs& a, int s, int h, int G) {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        const T* q = static_cast<const T*>(a.q) +
+                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            if (g < G) {
+                st.qb[ks][0] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * c);
+                st.qb[ks][1] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * c + 8);
+            } else {
+                st.qb[ks][0] = 0u;
+                st.qb[ks][1] = 0u;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) st.o[ks][r] = 0.f;
+        }
+        st.m[0] = st.m[1] = -INFINITY;
+        st.l[0] = st.l[1] = 0.f;
+    }
+
+    __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, uint8_t* kt, uint8_t* vt,
+                                         int n_valid, int, float*) {
+        const int lane = threadIdx.x & 31;
+        const int bs = a.block_size;
+        const uint32_t half_bytes = static_cast<uint32_t>(bs) * 128u;
+        // Rows past the valid tokens may hold anything (even NaN): zero the V
+        // rows so that 0 * V stays 0 in the PV product.
+        if (n_valid < bs) {
+            const int chunks = (bs - n_valid) * (D / 8);  // 16-byte chunks over both halves
+            for (int e = lane; e < chunks; e += 32) {
+                const int hf = e / ((bs - n_valid) * 8);
+                const int r = e - hf * (bs - n_valid) * 8;
+                uint4* p = reinterpret_cast<uint4*>(vt + hf * half_bytes +
+                                                    (n_valid + (r >> 3)) * 128 + ((r & 7) << 4));
+                *p = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+        const uint32_t kb = smem_addr(kt), vb = smem_addr(vt);
+        const uint32_t sw = lane & 7;  // 128-byte swizzle key of the rows this lane addresses
+        const float sl = a.scale_log2;
+        for (int mt = 0; mt < bs / 16; ++mt) {
+            // ---- S^T = K . Q^T for tokens 16mt .. 16mt+15
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const uint32_t row = static_cast<uint32_t>(mt * 16 + (lane & 7) + (lane & 8));
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const uint32_t chunk = ((ks & 3) << 1) | (lane >> 4);
+                    uint32_t af[4];
+                    ldsm_x4(af, kb + (ks >> 2) * half_bytes + row * 128u + ((chunk ^ sw) << 4));
+                    mma16816<DT>(acc, af, st.qb[ks][0], st.qb[ks][1]);
+                }
+            }
+            // ---- online softmax (heads 2c, 2c+1; tokens g and g+8 of the slice)
+            const int t0 = mt * 16 + (lane >> 2);
+            const bool v0 = t0 < n_valid, v1 = t0 + 8 < n_valid;
+            const float x0 = v0 ? acc[0] * sl : -INFINITY;
+            const float x1 = v0 ? acc[1] * sl : -INFINITY;
+            const float x2 = v1 ? acc[2] * sl : -INFINITY;
+            const float x3 = v1 ? acc[3] * sl : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+            const float al0 = fast_exp2(st.m[0] - mn0), al1 = fast_exp2(st.m[1] - mn1);
+            st.m[0] = mn0;
+            st.m[1] = mn1;
+            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+            st.l[0] = st.l[0] * al0 + (p0 + p2);
+            st.l[1] = st.l[1] * al1 + (p1 + p3);
+#pragma unroll
+            for (int mi = 0; mi < KS; ++mi) {
+                st.o[mi][0] *= al0;
+                st.o[mi][1] *= al1;
+                st.o[mi][2] *= al0;
+                st.o[mi][3] *= al1;
+            }
+            // ---- P^T fragments (k = token, n = head), high + low parts
+            uint32_t h01, l01, h23, l23;
+            pack_split<DT>(p0, p1, h01, l01);
+            pack_split<DT>(p2, p3, h23, l23);
+            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+            const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+            // ---- O^T += V^T . P^T
+            {
+                const uint32_t row = static_cast<uint32_t>(mt * 16 + (lane & 7) + ((lane >> 4) << 3));
+                const uint32_t csel = (lane >> 3) & 1;
+#pragma unroll
+                for (int mi = 0; mi < KS; ++mi) {
+                    const uint32_t chunk = ((mi & 3) << 1) | csel;
+                    uint32_t af[4];
+                    ldsm_x4_trans(af, vb + (mi >> 2) * half_bytes + row * 128u + ((chunk ^ sw) << 4));
+                    mma16816<DT>(st.o[mi], af, bh0, bh1);
+                    mma16816<DT>(st.o[mi], af, bl0, bl1);
+                }
+            }
+        }
+        if (n_valid < bs) fence_proxy_async_smem();  // generic writes before the next TMA fill
+    }
+
+    __device__ __forceinline__ void publish(const State& st, const DecodeArgs&, float* mw, int G) {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        float l0 = st.l[0], l1 = st.l[1];
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const int h0 = 2 * c, h1 = 2 * c + 1;
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+            const int d0 = 16 * mi + g;
+            if (h0 < G) {
+                mw[h0 * (D + 2) + d0] = st.o[mi][0];
+                mw[h0 * (D + 2) + d0 + 8] = st.o[mi][2];
+            }
+            if (h1 < G) {
+                mw[h1 * (D + 2) + d0] = st.o[mi][1];
+                mw[h1 * (D + 2) + d0 + 8] = st.o[mi][3];
+            }
+        }
+        if (g == 0) {
+            if (h0 < G) {
+                mw[h0 * (D + 2) + D] = st.m[0];
+                mw[h0 * (D + 2) + D + 1] = l0;
+            }
+            if (h1 < G) {
+                mw[h1 * (D + 2) + D] = st.m[1];
+                mw[h1 * (D + 2) + D + 1] = l1;
+            }
+        }
+    }
+};
+
+template <int DT, int D>
+static cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                cudaStream_t stream) {
+    return launch_partial<MmaPolicy<DT, D>>(a, tmk, tmv, stream);
+}
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              cudaStream_t stream) {
+    if (a.dtype == kF16) {
+        if (a.head_dim == 64) return launch_mma_t<kF16, 64>(a, tmk, tmv, stream);
+        if (a.head_dim == 128) return launch_mma_t<kF16, 128>(a, tmk, tmv, stream);
+    } else if (a.dtype == kBF16) {
+        if (a.head_dim == 64) return launch_mma_t<kBF16, 64>(a, tmk, tmv, stream);
+        if (a.head_dim == 128) return launch_mma_t<kBF16, 128>(a, tmk, tmv, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

@@ -1,0 +1,174 @@
+// Device helpers: mbarriers, bulk/tensor async copies (TMA), warp-level
+// tensor-core fragments, fast base-2 exponent, status flags.  Inline PTX
+// written for sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// Status bits (same values as KV_FLAG_* in pkv.h).
+constexpr uint32_t kFlagBadBlock = 0x1u;
+constexpr uint32_t kFlagBadSlot = 0x2u;
+constexpr uint32_t kFlagBadContext = 0x4u;
+constexpr uint32_t kFlagTimeout = 0x8u;
+
+// A bounded wait gives up after this many nanoseconds of the global timer.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ void raise_flag(uint32_t* status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete.  Gives up (returns false and
+// raises the timeout flag) after kWaitLimitNs, or at once if *abort is set.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                raise_flag(status, kFlagTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------- async bulk copies
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Contiguous global -> shared copy completed on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).  L2 evict-first: every tile is read once.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// 2-D tiled tensor copy (box given by the tensor map) completed on `bar`.
+__device__ __forceinline__ void tensor_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ----------------------------------------------------------- named barrier
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// --------------------------------------------------------------- math
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------- element load / convert
+template <int DT>
+struct Elem;
+template <>
+struct Elem<kF32> {
+    using T = float;
+    static __device__ __forceinline__ float to_float(T x) { return x; }
+    static __device__ __forceinline__ T from_float(float x) { return x; }
+};
+template <>
+struct Elem<kF16> {
+    using T = __half;
+    static __device__ __forceinline__ float to_float(T x) { return __half2float(x); }
+    static __device__ __forceinline__ T from_float(float x) { return __float2half_rn(x); }
+};
+template <>
+struct Elem<kBF16> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ float to_float(T x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ T from_float(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Store an fp32 value as out_dtype (round to nearest even).
+__device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int out_dtype) {
+    if (out_dtype == kF32)
+        static_cast<float*>(out)[idx] = v;
+    else if (out_dtype == kF16)
+        static_cast<__half*>(out)[idx] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+}  // namespace pkv

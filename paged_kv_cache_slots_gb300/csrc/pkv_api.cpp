@@ -1,0 +1,533 @@
+// C ABI of the paged KV cache library: validation, pool bookkeeping, launch
+// planning, tensor-map encoding and status handling.  Every argument is
+// checked here, before anything reaches the device.
+#include "pkv.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <mutex>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "pkv_internal.h"
+
+using namespace pkv;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+kv_status_t fail(kv_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kv_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(KV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool valid_dtype(int d) { return d == KV_F32 || d == KV_F16 || d == KV_BF16; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+int g_max_smem[kMaxDevices] = {};
+int g_smem_per_sm[kMaxDevices] = {};
+
+// Per-device facts and the status word of the current device.
+kv_status_t device_info(int* dev_out, uint32_t** status, int* sms, int* max_smem, int* smem_sm) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(KV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_status_ptr[dev] == nullptr) {
+        int v = 0;
+        if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        g_sm_count[dev] = v;
+        g_max_smem[dev] = max_dynamic_smem(dev);
+        if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(shared memory per SM)");
+        g_smem_per_sm[dev] = v;
+        uint32_t* p = nullptr;
+        if ((e = status_word_address(&p)) != cudaSuccess) return cuda_fail(e, "status word address");
+        g_status_ptr[dev] = p;
+    }
+    if (dev_out) *dev_out = dev;
+    if (status) *status = g_status_ptr[dev];
+    if (sms) *sms = g_sm_count[dev];
+    if (max_smem) *max_smem = g_max_smem[dev];
+    if (smem_sm) *smem_sm = g_smem_per_sm[dev];
+    return KV_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Options {
+    int num_ctas, ctas_per_sm, consumer_warps, kernel, test_stall;
+};
+
+kv_status_t read_options(const kv_decode_options_t* o, Options* out) {
+    Options r{0, 1, 8, KV_KERNEL_AUTO, 0};
+    if (o) {
+        if (o->num_ctas < 0 || o->ctas_per_sm < 0 || o->consumer_warps < 0 ||
+            o->consumer_warps > 15 || o->ctas_per_sm > 8)
+            return fail(KV_ERR_INVALID_ARG, "decode options out of range");
+        if (o->kernel != KV_KERNEL_AUTO && o->kernel != KV_KERNEL_FFMA && o->kernel != KV_KERNEL_MMA)
+            return fail(KV_ERR_INVALID_ARG, "unknown kernel selector %d", static_cast<int>(o->kernel));
+        if (o->num_ctas) r.num_ctas = o->num_ctas;
+        if (o->ctas_per_sm) r.ctas_per_sm = o->ctas_per_sm;
+        if (o->consumer_warps) r.consumer_warps = o->consumer_warps;
+        r.kernel = o->kernel;
+        r.test_stall = o->test_stall != 0;
+    }
+    *out = r;
+    return KV_OK;
+}
+
+int grid_size(const Options& o, int sms) { return o.num_ctas > 0 ? o.num_ctas : sms * o.ctas_per_sm; }
+
+size_t workspace_bytes_for(int num_seqs, int group, int num_kv_heads, int head_dim, int ctas) {
+    const size_t slots = static_cast<size_t>(ctas) + static_cast<size_t>(num_seqs) * num_kv_heads;
+    return align256(slots * group * head_dim * 4) + align256(slots * group * 2 * 4) +
+           align256(static_cast<size_t>(num_seqs + 1) * 4);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of one layer's cache: rows = num_blocks*Hkv*bs, row = head_dim
+// elements; box = 64 elements x block_size rows, 128-byte swizzle.
+kv_status_t encode_cache_map(CUtensorMap* map, const void* base, int dtype, int rows, int head_dim,
+                             int block_size) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(block_size)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return KV_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ pool
+struct kv_pool {
+    kv_pool_config_t cfg;
+    char* base;
+    bool owned;
+    size_t layer_bytes;  // one of K or V for one layer
+};
+
+// ---------------------------------------------------------------- allocator
+struct kv_block_allocator {
+    int num_blocks = 0, block_size = 0;
+    std::deque<int32_t> free_q;
+    struct Seq {
+        std::vector<int32_t> table;
+        int64_t tokens = 0;
+    };
+    std::unordered_map<int64_t, Seq> seqs;
+};
+
+extern "C" {
+
+const char* kv_status_string(kv_status_t s) {
+    switch (s) {
+        case KV_OK: return "KV_OK";
+        case KV_ERR_INVALID_ARG: return "KV_ERR_INVALID_ARG";
+        case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
+        case KV_ERR_OUT_OF_MEMORY: return "KV_ERR_OUT_OF_MEMORY";
+        case KV_ERR_OUT_OF_BLOCKS: return "KV_ERR_OUT_OF_BLOCKS";
+        case KV_ERR_WORKSPACE_TOO_SMALL: return "KV_ERR_WORKSPACE_TOO_SMALL";
+        case KV_ERR_CUDA: return "KV_ERR_CUDA";
+        case KV_ERR_DEVICE_CHECK: return "KV_ERR_DEVICE_CHECK";
+        case KV_ERR_DEVICE_TIMEOUT: return "KV_ERR_DEVICE_TIMEOUT";
+        case KV_ERR_NOT_FOUND: return "KV_ERR_NOT_FOUND";
+    }
+    return "KV_ERR_UNKNOWN";
+}
+
+const char* kv_last_error(void) { return g_last_error; }
+
+size_t kv_pool_bytes(const kv_pool_config_t* c) {
+    if (!c || c->num_layers <= 0 || c->num_blocks <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 ||
+        c->head_dim <= 0 || !valid_dtype(c->dtype))
+        return 0;
+    return 2ull * c->num_layers * c->num_blocks * c->block_size * c->num_kv_heads * c->head_dim *
+           static_cast<size_t>(dtype_bytes(c->dtype));
+}
+
+kv_status_t kv_pool_create(const kv_pool_config_t* cfg, void* buffer, size_t buffer_bytes,
+                           kv_pool_t** out) {
+    if (!cfg || !out) return fail(KV_ERR_INVALID_ARG, "kv_pool_create: null argument");
+    *out = nullptr;
+    const size_t bytes = kv_pool_bytes(cfg);
+    if (bytes == 0) return fail(KV_ERR_INVALID_ARG, "kv_pool_create: invalid configuration");
+    if (cfg->block_size > 1024) return fail(KV_ERR_INVALID_ARG, "block_size %d > 1024", cfg->block_size);
+    if ((static_cast<size_t>(cfg->head_dim) * dtype_bytes(cfg->dtype)) % 16)
+        return fail(KV_ERR_INVALID_ARG, "head_dim * element size must be a multiple of 16 bytes");
+    if (static_cast<int64_t>(cfg->num_blocks) * cfg->block_size >= (int64_t{1} << 31) ||
+        static_cast<int64_t>(cfg->num_blocks) * cfg->block_size * cfg->num_kv_heads >= (int64_t{1} << 31))
+        return fail(KV_ERR_UNSUPPORTED, "pool too large for 32-bit slot / row indices");
+    if (cfg->device < 0) return fail(KV_ERR_INVALID_ARG, "device %d", cfg->device);
+    if (buffer) {
+        if (buffer_bytes < bytes)
+            return fail(KV_ERR_INVALID_ARG, "buffer of %zu bytes < %zu needed", buffer_bytes, bytes);
+        if (!aligned(buffer, 256)) return fail(KV_ERR_INVALID_ARG, "pool buffer must be 256-byte aligned");
+    }
+    kv_pool* p = new (std::nothrow) kv_pool;
+    if (!p) return fail(KV_ERR_OUT_OF_MEMORY, "host allocation failed");
+    p->cfg = *cfg;
+    p->layer_bytes = bytes / (2ull * cfg->num_layers);
+    p->owned = buffer == nullptr;
+    p->base = static_cast<char*>(buffer);
+    if (!buffer) {
+        DeviceGuard g(cfg->device);
+        if (!g.ok) {
+            delete p;
+            return fail(KV_ERR_CUDA, "cannot select device %d", cfg->device);
+        }
+        void* mem = nullptr;
+        cudaError_t e = cudaMalloc(&mem, bytes);
+        if (e != cudaSuccess) {
+            delete p;
+            cudaGetLastError();
+            return fail(KV_ERR_OUT_OF_MEMORY, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+        }
+        p->base = static_cast<char*>(mem);
+    }
+    *out = p;
+    return KV_OK;
+}
+
+void kv_pool_destroy(kv_pool_t* p) {
+    if (!p) return;
+    if (p->owned && p->base) {
+        DeviceGuard g(p->cfg.device);
+        cudaFree(p->base);
+    }
+    delete p;
+}
+
+kv_status_t kv_pool_layer(const kv_pool_t* p, int layer, void** k, void** v) {
+    if (!p || !k || !v) return fail(KV_ERR_INVALID_ARG, "kv_pool_layer: null argument");
+    if (layer < 0 || layer >= p->cfg.num_layers)
+        return fail(KV_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, p->cfg.num_layers);
+    *k = p->base + (2ull * layer) * p->layer_bytes;
+    *v = p->base + (2ull * layer + 1) * p->layer_bytes;
+    return KV_OK;
+}
+
+kv_status_t kv_pool_config(const kv_pool_t* p, kv_pool_config_t* c) {
+    if (!p || !c) return fail(KV_ERR_INVALID_ARG, "kv_pool_config: null argument");
+    *c = p->cfg;
+    return KV_OK;
+}
+
+kv_status_t kv_slot_mapping(const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                            int num_seqs, int block_size, int num_blocks, int32_t* slot_mapping,
+                            void* stream) {
+    if (num_seqs < 0 || max_blocks <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(KV_ERR_INVALID_ARG, "kv_slot_mapping: sizes out of range");
+    if (num_seqs == 0) return KV_OK;
+    if (!block_tables || !context_lens || !slot_mapping)
+        return fail(KV_ERR_INVALID_ARG, "kv_slot_mapping: null pointer");
+    if (static_cast<int64_t>(num_blocks) * block_size >= (int64_t{1} << 31))
+        return fail(KV_ERR_UNSUPPORTED, "slots do not fit in int32");
+    uint32_t* status = nullptr;
+    if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
+    SlotArgs a{block_tables, context_lens, slot_mapping, status, max_blocks, num_seqs, block_size, num_blocks};
+    cudaError_t e = launch_slot_mapping(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "slot mapping launch");
+    return KV_OK;
+}
+
+kv_status_t kv_append(kv_pool_t* p, int layer, const int32_t* seq_ids, int n_tokens, const void* k,
+                      const void* v, const int32_t* slot_mapping, void* stream) {
+    if (!p) return fail(KV_ERR_INVALID_ARG, "kv_append: null pool");
+    if (n_tokens < 0) return fail(KV_ERR_INVALID_ARG, "kv_append: n_tokens %d", n_tokens);
+    void *kc = nullptr, *vc = nullptr;
+    if (kv_status_t st = kv_pool_layer(p, layer, &kc, &vc)) return st;
+    if (n_tokens == 0) return KV_OK;
+    if (!k || !v || !slot_mapping) return fail(KV_ERR_INVALID_ARG, "kv_append: null pointer");
+    if (!aligned(k, 16) || !aligned(v, 16))
+        return fail(KV_ERR_INVALID_ARG, "kv_append: k and v must be 16-byte aligned");
+    if (static_cast<int64_t>(n_tokens) * p->cfg.num_kv_heads >= (int64_t{1} << 31) / 32)
+        return fail(KV_ERR_UNSUPPORTED, "kv_append: too many tokens in one call");
+    uint32_t* status = nullptr;
+    if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
+    AppendArgs a{seq_ids, k, v, slot_mapping, kc, vc, status, n_tokens, p->cfg.num_kv_heads,
+                 p->cfg.head_dim, p->cfg.block_size, p->cfg.num_blocks, dtype_bytes(p->cfg.dtype)};
+    cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return KV_OK;
+}
+
+kv_status_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                         int device, const kv_decode_options_t* opts, size_t* bytes) {
+    if (!bytes) return fail(KV_ERR_INVALID_ARG, "null bytes_out");
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        num_q_heads % num_kv_heads)
+        return fail(KV_ERR_INVALID_ARG, "workspace: sizes out of range");
+    Options o;
+    if (kv_status_t st = read_options(opts, &o)) return st;
+    int sms = 0;
+    if (o.num_ctas <= 0) {
+        DeviceGuard g(device);
+        if (!g.ok) return fail(KV_ERR_CUDA, "cannot select device %d", device);
+        if (kv_status_t st = device_info(nullptr, nullptr, &sms, nullptr, nullptr)) return st;
+    }
+    *bytes = workspace_bytes_for(num_seqs, num_q_heads / num_kv_heads, num_kv_heads, head_dim,
+                                 grid_size(o, sms));
+    return KV_OK;
+}
+
+kv_status_t paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, kv_dtype_t dtype, float scale, void* out,
+                                   kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                                   const kv_decode_options_t* opts, void* stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
+        return fail(KV_ERR_INVALID_ARG, "paged_decode_attention: sizes out of range");
+    if (num_q_heads % num_kv_heads)
+        return fail(KV_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                    num_kv_heads);
+    const int G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(KV_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", G);
+    if (head_dim != 64 && head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+    if (block_size < 1 || block_size > 256) return fail(KV_ERR_UNSUPPORTED, "block_size %d", block_size);
+    if (!valid_dtype(dtype) || !valid_dtype(out_dtype))
+        return fail(KV_ERR_INVALID_ARG, "unknown dtype");
+    if (out_dtype != KV_F32 && out_dtype != dtype)
+        return fail(KV_ERR_UNSUPPORTED, "out_dtype must be KV_F32 or the input dtype");
+    if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale is not finite");
+    if (static_cast<int64_t>(num_seqs) * num_kv_heads * max_blocks >= (int64_t{1} << 31) ||
+        static_cast<int64_t>(num_blocks) * num_kv_heads * block_size >= (int64_t{1} << 31))
+        return fail(KV_ERR_UNSUPPORTED, "sizes exceed 32-bit tile / row indices");
+    Options o;
+    if (kv_status_t st = read_options(opts, &o)) return st;
+    int kernel = o.kernel;
+    const bool mma_ok = (dtype == KV_F16 || dtype == KV_BF16) && block_size % 16 == 0;
+    if (kernel == KV_KERNEL_AUTO) kernel = mma_ok ? KV_KERNEL_MMA : KV_KERNEL_FFMA;
+    if (kernel == KV_KERNEL_MMA && !mma_ok)
+        return fail(KV_ERR_UNSUPPORTED, "tensor-core kernel needs f16/bf16 and block_size % 16 == 0");
+    if (num_seqs == 0) return KV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+        return fail(KV_ERR_INVALID_ARG, "paged_decode_attention: null pointer");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 256))
+        return fail(KV_ERR_INVALID_ARG,
+                    "alignment: caches, q and out need 16 bytes, the workspace 256 bytes");
+    int dev = 0, sms = 0, max_smem = 0, smem_sm = 0;
+    uint32_t* status = nullptr;
+    if (kv_status_t st = device_info(&dev, &status, &sms, &max_smem, &smem_sm)) return st;
+    const int P = grid_size(o, sms);
+    const size_t need = workspace_bytes_for(num_seqs, G, num_kv_heads, head_dim, P);
+    if (workspace_bytes < need)
+        return fail(KV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    int budget = max_smem;
+    if (o.ctas_per_sm > 1) {
+        const int share = smem_sm / o.ctas_per_sm - 1024;
+        if (share < budget) budget = share;
+    }
+    DecodePlan plan{};
+    if (!decode_plan(kernel, dtype, head_dim, block_size, G, num_seqs, o.consumer_warps, budget, &plan))
+        return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages for these sizes");
+
+    char* ws = static_cast<char*>(workspace);
+    const size_t slots = static_cast<size_t>(P) + static_cast<size_t>(num_seqs) * num_kv_heads;
+    DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = out;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_ml = reinterpret_cast<float*>(ws + align256(slots * G * head_dim * 4));
+    a.cum = reinterpret_cast<int32_t*>(ws + align256(slots * G * head_dim * 4) + align256(slots * G * 2 * 4));
+    a.status = status;
+    a.num_blocks = num_blocks;
+    a.max_blocks = max_blocks;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.dtype = dtype;
+    a.out_dtype = out_dtype;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.num_ctas = P;
+    a.consumer_warps = o.consumer_warps;
+    a.stages = plan.stages;
+    a.smem_bytes = plan.smem_bytes;
+    a.test_stall = o.test_stall;
+    a.device = dev;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (kernel == KV_KERNEL_MMA) {
+        CUtensorMap tk, tv;
+        const int rows = num_blocks * num_kv_heads * block_size;
+        if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, block_size)) return st;
+        if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, block_size)) return st;
+        e = launch_decode_mma(a, tk, tv, s);
+    } else {
+        e = launch_decode_ffma(a, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "decode partial launch");
+    e = launch_decode_reduce(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode reduce launch");
+    return KV_OK;
+}
+
+kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out) {
+    DeviceGuard g(device);
+    if (!g.ok) return fail(KV_ERR_CUDA, "cannot select device %d", device);
+    uint32_t* status = nullptr;
+    if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t flags = 0;
+    if ((e = cudaMemcpy(&flags, status, sizeof flags, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "reading the status word");
+    if (flags && (e = cudaMemset(status, 0, sizeof flags)) != cudaSuccess)
+        return cuda_fail(e, "clearing the status word");
+    if (flags_out) *flags_out = flags;
+    if (!flags) return KV_OK;
+    if (flags & KV_FLAG_TIMEOUT) return fail(KV_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
+    return fail(KV_ERR_DEVICE_CHECK, "device check flags 0x%x", flags);
+}
+
+// ------------------------------------------------------------ allocator
+kv_status_t kv_allocator_create(int num_blocks, int block_size, int reserve_null_block,
+                                kv_block_allocator_t** out) {
+    if (!out) return fail(KV_ERR_INVALID_ARG, "null out");
+    *out = nullptr;
+    if (num_blocks <= 0 || block_size <= 0) return fail(KV_ERR_INVALID_ARG, "allocator sizes");
+    kv_block_allocator* a = new (std::nothrow) kv_block_allocator;
+    if (!a) return fail(KV_ERR_OUT_OF_MEMORY, "host allocation failed");
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    for (int b = reserve_null_block ? 1 : 0; b < num_blocks; ++b) a->free_q.push_back(b);
+    *out = a;
+    return KV_OK;
+}
+
+void kv_allocator_destroy(kv_block_allocator_t* a) { delete a; }
+
+kv_status_t kv_allocator_extend(kv_block_allocator_t* a, int64_t seq_id, int new_tokens) {
+    if (!a || new_tokens < 0) return fail(KV_ERR_INVALID_ARG, "kv_allocator_extend arguments");
+    auto it = a->seqs.find(seq_id);
+    const int64_t have_tokens = it == a->seqs.end() ? 0 : it->second.tokens;
+    const size_t have_blocks = it == a->seqs.end() ? 0 : it->second.table.size();
+    const int64_t total = have_tokens + new_tokens;
+    const int64_t need_blocks = (total + a->block_size - 1) / a->block_size - static_cast<int64_t>(have_blocks);
+    if (need_blocks > static_cast<int64_t>(a->free_q.size()))
+        return fail(KV_ERR_OUT_OF_BLOCKS, "sequence %lld needs %lld blocks, %zu free",
+                    static_cast<long long>(seq_id), static_cast<long long>(need_blocks), a->free_q.size());
+    auto& s = a->seqs[seq_id];
+    for (int64_t i = 0; i < need_blocks; ++i) {
+        s.table.push_back(a->free_q.front());
+        a->free_q.pop_front();
+    }
+    s.tokens = total;
+    return KV_OK;
+}
+
+kv_status_t kv_allocator_release(kv_block_allocator_t* a, int64_t seq_id) {
+    if (!a) return fail(KV_ERR_INVALID_ARG, "null allocator");
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return fail(KV_ERR_NOT_FOUND, "unknown sequence %lld", static_cast<long long>(seq_id));
+    for (int32_t b : it->second.table) a->free_q.push_back(b);
+    a->seqs.erase(it);
+    return KV_OK;
+}
+
+kv_status_t kv_allocator_table(const kv_block_allocator_t* a, int64_t seq_id, int32_t* table_out,
+                               int capacity, int* num_blocks_out, int* num_tokens_out) {
+    if (!a || capacity < 0 || (capacity > 0 && !table_out)) return fail(KV_ERR_INVALID_ARG, "kv_allocator_table arguments");
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return fail(KV_ERR_NOT_FOUND, "unknown sequence %lld", static_cast<long long>(seq_id));
+    const auto& t = it->second.table;
+    if (static_cast<int>(t.size()) > capacity && table_out)
+        return fail(KV_ERR_INVALID_ARG, "table of %zu blocks does not fit in %d entries", t.size(), capacity);
+    for (size_t i = 0; i < t.size() && table_out; ++i) table_out[i] = t[i];
+    if (num_blocks_out) *num_blocks_out = static_cast<int>(t.size());
+    if (num_tokens_out) *num_tokens_out = static_cast<int>(it->second.tokens);
+    return KV_OK;
+}
+
+kv_status_t kv_allocator_slot(const kv_block_allocator_t* a, int64_t seq_id, int position, int32_t* slot_out) {
+    if (!a || !slot_out) return fail(KV_ERR_INVALID_ARG, "kv_allocator_slot arguments");
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return fail(KV_ERR_NOT_FOUND, "unknown sequence %lld", static_cast<long long>(seq_id));
+    const auto& t = it->second.table;
+    if (position < 0 || static_cast<int64_t>(position) >= static_cast<int64_t>(t.size()) * a->block_size)
+        return fail(KV_ERR_INVALID_ARG, "position %d outside the sequence's blocks", position);
+    *slot_out = t[position / a->block_size] * a->block_size + position % a->block_size;
+    return KV_OK;
+}
+
+kv_status_t kv_allocator_free_queue(const kv_block_allocator_t* a, int32_t* out, int capacity, int* count_out) {
+    if (!a || capacity < 0 || (capacity > 0 && !out)) return fail(KV_ERR_INVALID_ARG, "kv_allocator_free_queue arguments");
+    const int n = static_cast<int>(a->free_q.size());
+    if (count_out) *count_out = n;
+    if (out) {
+        if (n > capacity) return fail(KV_ERR_INVALID_ARG, "free queue of %d does not fit in %d", n, capacity);
+        int i = 0;
+        for (int32_t b : a->free_q) out[i++] = b;
+    }
+    return KV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Internal interface between the C-ABI host layer (pkv_api.cpp) and the CUDA
+// launchers (*.cu).  Plain structs of pointers and sizes; no torch types.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Element types as stored in the pool, q and out (same codes as kv_dtype_t).
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+__host__ __device__ inline int dtype_bytes(int dt) { return dt == kF32 ? 4 : 2; }
+
+struct AppendArgs {
+    const int32_t* seq_ids;       // [n_tokens] or nullptr
+    const void* k;                // [n_tokens][Hkv][D]
+    const void* v;
+    const int32_t* slot_mapping;  // [n_tokens]
+    void* k_cache;                // [NB][Hkv][bs][D]
+    void* v_cache;
+    uint32_t* status;             // device status word
+    int n_tokens, num_kv_heads, head_dim, block_size, num_blocks, elem_bytes;
+};
+
+struct SlotArgs {
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t* slot_mapping;
+    uint32_t* status;
+    int max_blocks, num_seqs, block_size, num_blocks;
+};
+
+// Everything the split-context decode kernels need.  The flattened work space
+// is the (sequence, kv head, logical block) triples in that order; CTA c of
+// num_ctas owns [c*W/P, (c+1)*W/P) of it.
+struct DecodeArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    void* out;
+    float* part_o;    // [slots][G][D]    unnormalised partial outputs
+    float* part_ml;   // [slots][G][2]    running max (log2 units) and sum
+    int32_t* cum;     // [num_seqs + 1]   exclusive prefix of tiles per sequence
+    uint32_t* status;
+    int num_blocks, max_blocks, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+    int dtype, out_dtype;
+    float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+    int num_ctas, consumer_warps, stages;
+    int smem_bytes;
+    int test_stall;  // testing only: see kv_decode_options_t
+    int device;      // CUDA ordinal the launch targets
+};
+
+// Shared-memory plan of the partial kernel.
+struct DecodePlan {
+    int stages;
+    int smem_bytes;
+    int tile_bytes;  // one (block, kv head) tile of K (same for V)
+};
+
+bool decode_plan(int kernel, int dtype, int head_dim, int block_size, int group, int num_seqs,
+                 int consumer_warps, int smem_budget, DecodePlan* plan);
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_slot_mapping(const SlotArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_ffma(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, cudaStream_t stream);
+cudaError_t launch_decode_reduce(const DecodeArgs& a, cudaStream_t stream);
+
+// Largest dynamic shared memory a CTA may request on `device`.
+int max_dynamic_smem(int device);
+
+// Device address of the current device's status word.
+cudaError_t status_word_address(uint32_t** ptr);
+
+}  // namespace pkv

@@ -1,0 +1,159 @@
+"""Helpers of the GPU parity tests.
+
+Inputs come from `workloads` only.  The CUDA side runs through the library's
+C ABI (via the Python binding); the expected values come from `oracle` only,
+computed on the host from the same inputs (the pre-append pool, the new rows,
+the tables).  Nothing computed by the CUDA path is fed to the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_slots_gb300 as pkv
+from workloads import fill_pool_layer, pool_layer_values, step_layer_values
+
+# max |out - oracle| for fp32 output (fp16/bf16 inputs, fp32 accumulation).
+ATOL = 2e-3
+
+
+def bits(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int32) if t.element_size() == 4 else t.view(torch.int16)
+
+
+def half_ulp(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """Half a unit in the last place of `dtype` at |ref| (rounding of the final cast)."""
+    if dtype == torch.float32:
+        return np.abs(ref) * 2.0 ** -24
+    mant = 10 if dtype == torch.float16 else 7
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -14)))
+    return 2.0 ** (e - mant - 1)
+
+
+def check_output(out: torch.Tensor, ref: np.ndarray, what: str):
+    got = out.detach().float().cpu().double().numpy()
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = ATOL + (0 if out.dtype == torch.float32 else half_ulp(ref, out.dtype))
+    worst = float(np.max(err - bound)) if err.size else -1.0
+    assert worst <= 0, f"{what}: max |err| {float(err.max()):.3e} exceeds bound by {worst:.3e}"
+    return float(err.max()) if err.size else 0.0
+
+
+def newest_slot_masks(placement):
+    """seq_ids passed to the append: -1 marks a sequence that writes nothing."""
+    return np.where(placement.appends, np.arange(len(placement.appends)), -1).astype(np.int32)
+
+
+class SmallCase:
+    """A workload small enough that the oracle checks every output; host copies kept."""
+
+    def __init__(self, spec, placement, layer=0):
+        self.spec, self.pl, self.layer = spec, placement, layer
+        self.kpool, self.vpool = pool_layer_values(spec, placement.num_blocks, layer, "cpu")
+        self.q, self.kn, self.vn = step_layer_values(spec, len(placement.context_lens), layer, "cpu")
+
+    def oracle(self):
+        """(slots, K after append, V after append, fp64 attention output)."""
+        sl = oracle.slot_mapping(self.pl.block_tables, self.pl.context_lens, self.spec.block_size)
+        sl_w = np.where(self.pl.appends, sl, -1).astype(np.int32)
+        kpost, vpost = oracle.append(self.kpool, self.vpool, self.kn, self.vn, sl_w)
+        ref = oracle.paged_decode(self.q, kpost, vpost, self.pl.block_tables, self.pl.context_lens,
+                                  self.spec.attn_scale)
+        return sl, kpost, vpost, ref
+
+    def device(self, dev="cuda"):
+        s = self.spec
+        pool = pkv.KVPool(s.num_layers, self.pl.num_blocks, s.block_size, s.num_kv_heads,
+                          s.head_dim, s.torch_dtype, device=dev)
+        kc, vc = pool.layer(self.layer)
+        kc.copy_(self.kpool)
+        vc.copy_(self.vpool)
+        d = dict(pool=pool, kc=kc, vc=vc,
+                 tables=torch.from_numpy(self.pl.block_tables).to(dev),
+                 ctx=torch.from_numpy(self.pl.context_lens).to(dev),
+                 seq_ids=torch.from_numpy(newest_slot_masks(self.pl)).to(dev),
+                 q=self.q.to(dev), kn=self.kn.to(dev), vn=self.vn.to(dev))
+        return d
+
+
+def run_step(d, spec, num_blocks, layer=0, out_dtype=None, **opts):
+    """Slot mapping, append and attention of one layer through the library."""
+    slots = pkv.slot_mapping(d["tables"], d["ctx"], spec.block_size, num_blocks)
+    d["pool"].append(layer, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
+    out = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
+                                     spec.attn_scale, out_dtype=out_dtype, **opts)
+    return slots, out
+
+
+def compact_blocks(tables: np.ndarray, seqs) -> tuple[np.ndarray, np.ndarray]:
+    """Physical blocks used by `seqs` and their tables renumbered into that list."""
+    rows = tables[seqs]
+    used = np.unique(rows[rows >= 0])
+    remap = np.full(int(tables.max()) + 1, -1, dtype=np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    new = np.where(rows >= 0, remap[np.maximum(rows, 0)], -1).astype(np.int32)
+    return used, new
+
+
+class LargeCase:
+    """A full-size workload generated on the device; the oracle checks sampled sequences."""
+
+    def __init__(self, spec, placement, dev="cuda"):
+        self.spec, self.pl, self.dev = spec, placement, dev
+        s = spec
+        self.pool = pkv.KVPool(s.num_layers, placement.num_blocks, s.block_size, s.num_kv_heads,
+                               s.head_dim, s.torch_dtype, device=dev)
+        self.tables = torch.from_numpy(placement.block_tables).to(dev)
+        self.ctx = torch.from_numpy(placement.context_lens).to(dev)
+        self.seq_ids = torch.from_numpy(newest_slot_masks(placement)).to(dev)
+
+    def fill(self, layer):
+        kc, vc = self.pool.layer(layer)
+        fill_pool_layer(self.spec, layer, kc, vc)
+        q, kn, vn = step_layer_values(self.spec, len(self.pl.context_lens), layer, self.dev)
+        return kc, vc, q, kn, vn
+
+    def check_layer(self, layer, seqs, **opts):
+        """Run one layer on the full batch; compare sampled sequences with the oracle."""
+        s, pl = self.spec, self.pl
+        kc, vc, q, kn, vn = self.fill(layer)
+        used, ctab = compact_blocks(pl.block_tables, seqs)
+        used_t = torch.from_numpy(used.astype(np.int64)).to(self.dev)
+        k_pre, v_pre = kc[used_t].cpu(), vc[used_t].cpu()  # the oracle's pool: pre-append
+        slots = pkv.slot_mapping(self.tables, self.ctx, s.block_size, pl.num_blocks)
+        self.pool.append(layer, kn, vn, slots, seq_ids=self.seq_ids)
+        out32 = pkv.paged_decode_attention(q, kc, vc, self.tables, self.ctx, s.attn_scale,
+                                           out_dtype=torch.float32, **opts)
+        outq = pkv.paged_decode_attention(q, kc, vc, self.tables, self.ctx, s.attn_scale, **opts)
+        st, flags = pkv.device_status()
+        assert st == 0 and flags == 0, f"device status {st} flags {flags:#x}"
+        # Oracle on the sampled sequences, over the compact pool.
+        ctx_s = pl.context_lens[seqs]
+        o_sl = oracle.slot_mapping(ctab, ctx_s, s.block_size)
+        o_sl = np.where(pl.appends[seqs], o_sl, -1).astype(np.int32)
+        kn_s, vn_s, q_s = kn[seqs].cpu(), vn[seqs].cpu(), q[seqs].cpu()
+        k_post, v_post = oracle.append(k_pre, v_pre, kn_s, vn_s, o_sl)
+        ref = oracle.paged_decode(q_s, k_post, v_post, ctab, ctx_s, s.attn_scale)
+        # Append: every sampled block bit-exact after the step.
+        assert torch.equal(bits(kc[used_t].cpu()), bits(k_post)), "K blocks after append"
+        assert torch.equal(bits(vc[used_t].cpu()), bits(v_post)), "V blocks after append"
+        # Device slot mapping: bit-exact for the sampled sequences (real table).
+        o_full = oracle.slot_mapping(pl.block_tables[seqs], ctx_s, s.block_size)
+        assert np.array_equal(slots.cpu().numpy()[seqs], o_full), "slot mapping"
+        idx = torch.as_tensor(seqs, device=self.dev)
+        e32 = check_output(out32[idx], ref, f"{s.name} layer {layer} fp32 out")
+        eq = check_output(outq[idx], ref, f"{s.name} layer {layer} {s.dtype} out")
+        return e32, eq
+
+
+def sample_sequences(placement, n, seed):
+    """n sequences: the longest, the shortest, and a seeded draw of the rest."""
+    ctx = placement.context_lens
+    order = np.argsort(ctx, kind="stable")
+    pick = {int(order[0]), int(order[-1])}
+    rng = np.random.default_rng(seed)
+    rest = [i for i in range(len(ctx)) if i not in pick]
+    pick.update(int(x) for x in rng.choice(rest, size=min(n - len(pick), len(rest)), replace=False))
+    return np.array(sorted(pick), dtype=np.int64)

@@ -1,0 +1,272 @@
+"""GPU parity of the CUDA path against the oracle (runs through the C ABI).
+
+Bars: append and slot mapping bit-exact; attention max |err| <= 2e-3 against
+the fp64 oracle with fp32 output, and the same plus half an ulp of the output
+type for fp16/bf16 output.  Small workloads are checked on every output; the
+full-size workloads (in the launch configuration the benchmark times) on
+sampled sequences of the first and last layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_slots_gb300 as pkv
+from gpu_harness import (LargeCase, SmallCase, bits, check_output, run_step, sample_sequences)
+from workloads import SPECS, make_placement, small_spec
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _full_small_check(spec, placement=None, kernels=("auto",), **opts):
+    pl = placement or make_placement(spec)
+    case = SmallCase(spec, pl)
+    o_slots, kpost, vpost, ref = case.oracle()
+    errs = {}
+    for kernel in kernels:
+        d = case.device()
+        slots, out = run_step(d, spec, pl.num_blocks, out_dtype=torch.float32, kernel=kernel, **opts)
+        outq = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
+                                          spec.attn_scale, kernel=kernel, **opts)
+        st, flags = pkv.device_status()
+        assert st == 0 and flags == 0, (st, flags)
+        assert np.array_equal(slots.cpu().numpy(), o_slots), "slot mapping"
+        assert torch.equal(bits(d["kc"].cpu()), bits(kpost)), "K pool after append"
+        assert torch.equal(bits(d["vc"].cpu()), bits(vpost)), "V pool after append"
+        e32 = check_output(out, ref, f"{spec.name}/{kernel} fp32 out")
+        eq = check_output(outq, ref, f"{spec.name}/{kernel} {spec.dtype} out")
+        errs[kernel] = (e32, eq)
+    return errs
+
+
+def test_tiny_fp32_every_output():
+    _full_small_check(SPECS["tiny"], kernels=("auto", "ffma"))
+
+
+@pytest.mark.parametrize("kernel", ["mma", "ffma"])
+def test_llama8b_layer_b8_every_output(kernel):
+    _full_small_check(SPECS["llama8b_layer_b8"], kernels=(kernel,))
+
+
+def test_batch32_32_layers_sampled():
+    spec = SPECS["llama8b_32l_b32"]
+    case = LargeCase(spec, make_placement(spec))
+    seqs = sample_sequences(case.pl, 6, seed=20)
+    for layer in (0, spec.num_layers - 1):
+        case.check_layer(layer, seqs)
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_mixed_prefix_b64_sampled():
+    spec = SPECS["mixed_prefix_b64"]
+    pl = make_placement(spec)
+    case = LargeCase(spec, pl)
+    # Two whole prefix groups (shared blocks, some members that do not append)
+    # plus the longest and shortest sequences.
+    seqs = np.unique(np.concatenate([np.arange(0, 8), np.arange(24, 32), sample_sequences(pl, 2, 3)]))
+    case.check_layer(0, seqs)
+    # Members of a group that share a table prefix read identical blocks.
+    assert (pl.block_tables[0, :8] == pl.block_tables[1, :8]).all()
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_serving_b256_sampled():
+    spec = SPECS["serving_b256"]
+    case = LargeCase(spec, make_placement(spec))
+    seqs = sample_sequences(case.pl, 12, seed=40)
+    for layer in (0, spec.num_layers - 1):
+        case.check_layer(layer, seqs)
+    del case
+    torch.cuda.empty_cache()
+
+
+EDGE_CTX = (1, 15, 16, 17, 31, 32, 33, 0, 100)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_edge_lengths_all_shapes(dtype, head_dim, group):
+    spec = small_spec(f"edge_{dtype}_{head_dim}_{group}", num_q_heads=2 * group, num_kv_heads=2,
+                      head_dim=head_dim, block_size=16, dtype=dtype, seed=head_dim + group,
+                      ctx=EDGE_CTX)
+    kernels = ("ffma",) if dtype == "f32" else ("mma", "ffma")
+    _full_small_check(spec, kernels=kernels)
+
+
+@pytest.mark.parametrize("block_size", [32, 48, 64])
+def test_other_block_sizes(block_size):
+    spec = small_spec(f"bs{block_size}", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                      block_size=block_size, dtype="bf16", seed=block_size,
+                      ctx=(1, block_size - 1, block_size, block_size + 1, 5 * block_size + 3))
+    _full_small_check(spec, kernels=("mma", "ffma"))
+
+
+def test_block_size_8_uses_the_ffma_kernel():
+    spec = small_spec("bs8", num_q_heads=4, num_kv_heads=1, head_dim=64, block_size=8, dtype="f16",
+                      seed=8, ctx=(1, 7, 8, 9, 70))
+    _full_small_check(spec, kernels=("auto", "ffma"))
+
+
+@pytest.mark.parametrize("kernel", ["mma", "ffma"])
+def test_split_and_warp_counts_agree(kernel):
+    """Any persistent-grid size or consumer-warp count gives the same result."""
+    spec = small_spec("splits", num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16,
+                      dtype="f16", seed=5, ctx=(700, 1, 333, 2048, 16, 45))
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    _, _, _, ref = case.oracle()
+    d = case.device()
+    slots = pkv.slot_mapping(d["tables"], d["ctx"], spec.block_size, pl.num_blocks)
+    d["pool"].append(0, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
+    outs = []
+    for num_ctas, warps in [(0, 0), (1, 8), (2, 1), (7, 3), (64, 8), (1000, 15), (152, 4)]:
+        out = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
+                                         spec.attn_scale, out_dtype=torch.float32, kernel=kernel,
+                                         num_ctas=num_ctas, consumer_warps=warps)
+        check_output(out, ref, f"num_ctas={num_ctas} warps={warps}")
+        outs.append(out)
+    for o in outs[1:]:
+        assert torch.max(torch.abs(o - outs[0])).item() <= 2e-5
+    assert pkv.device_status() == (0, 0)
+
+
+@pytest.mark.parametrize("kernel", ["mma", "ffma"])
+def test_block_relabelling_is_bitwise_invariant(kernel):
+    spec = small_spec("relabel", num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                      dtype="bf16", seed=9, ctx=(300, 17, 64, 1))
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    d = case.device()
+    base = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                                      kernel=kernel)
+    perm = torch.randperm(pl.num_blocks, generator=torch.Generator().manual_seed(3))
+    kc2, vc2 = torch.empty_like(d["kc"]), torch.empty_like(d["vc"])
+    kc2[perm.cuda()] = d["kc"]
+    vc2[perm.cuda()] = d["vc"]
+    t = torch.from_numpy(pl.block_tables).long()
+    t2 = torch.where(t >= 0, perm[t.clamp(min=0)], torch.full_like(t, -1)).int().cuda()
+    out = pkv.paged_decode_attention(d["q"], kc2, vc2, t2, d["ctx"], spec.attn_scale, kernel=kernel)
+    assert torch.equal(bits(out), bits(base))
+
+
+@pytest.mark.parametrize("kernel", ["mma", "ffma"])
+def test_equal_heads_and_shared_tables(kernel):
+    spec = small_spec("equal", num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
+                      dtype="f16", seed=10, ctx=(130, 130, 40))
+    pl = make_placement(spec)
+    pl.block_tables[1] = pl.block_tables[0]  # sequence 1 reads sequence 0's blocks
+    case = SmallCase(spec, pl)
+    d = case.device()
+    q = d["q"].clone()
+    q[:, 1] = q[:, 0]
+    q[1] = q[0]
+    out = pkv.paged_decode_attention(q, d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                                     kernel=kernel)
+    assert torch.equal(bits(out[:, 1]), bits(out[:, 0]))
+    assert torch.equal(bits(out[1]), bits(out[0]))
+    ref = oracle.paged_decode(q.cpu(), case.kpool, case.vpool, pl.block_tables, pl.context_lens,
+                              spec.attn_scale)
+    check_output(out, ref, "shared tables")
+
+
+def test_nan_in_unused_slots_does_not_leak():
+    """Slots past a sequence's length may hold anything; the output ignores them."""
+    spec = small_spec("nan", num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                      dtype="bf16", seed=12, ctx=(5, 17, 33))
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    for s, c in enumerate(pl.context_lens):
+        last = pl.block_tables[s, (c - 1) // 16]
+        case.kpool[last, :, c % 16 or 16:, :] = float("nan")
+        case.vpool[last, :, c % 16 or 16:, :] = float("nan")
+    _, _, _, ref = case.oracle()
+    for kernel in ("mma", "ffma"):
+        d = case.device()
+        _, out = run_step(d, spec, pl.num_blocks, out_dtype=torch.float32, kernel=kernel)
+        check_output(out, ref, f"NaN-padded blocks ({kernel})")
+
+
+def test_device_checks_flag_and_continue():
+    spec = small_spec("checks", num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+                      dtype="f16", seed=13, ctx=(40, 20))
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    d = case.device()
+    assert pkv.device_status() == (0, 0)
+    bad = d["tables"].clone()
+    bad[0, 1] = pl.num_blocks + 5  # outside the pool
+    pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], bad, d["ctx"], spec.attn_scale)
+    st, flags = pkv.device_status()
+    assert st == 7 and flags & pkv.FLAG_BAD_BLOCK_ID
+    assert pkv.device_status() == (0, 0)  # read and cleared
+    slots = torch.tensor([pl.num_blocks * 16 + 3, -1], dtype=torch.int32, device="cuda")
+    before = d["kc"].clone()
+    d["pool"].append(0, d["kn"], d["vn"], slots)
+    st, flags = pkv.device_status()
+    assert st == 7 and flags == pkv.FLAG_BAD_SLOT
+    assert torch.equal(bits(before), bits(d["kc"]))  # nothing written
+    long_ctx = torch.tensor([40, 10_000], dtype=torch.int32, device="cuda")
+    pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], long_ctx, spec.attn_scale)
+    st, flags = pkv.device_status()
+    assert st == 7 and flags & pkv.FLAG_BAD_CONTEXT
+    # The context stays usable: a clean call afterwards is still exact.
+    _full_small_check(spec, pl)
+
+
+def test_bounded_wait_times_out_cleanly():
+    """A stalled producer makes a consumer's bounded wait run out: status, no fault."""
+    spec = small_spec("stall", num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                      dtype="bf16", seed=14, ctx=(200, 300))
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    d = case.device()
+    pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                               num_ctas=1, test_stall=True)
+    st, flags = pkv.device_status()
+    assert st == 8 and flags & pkv.FLAG_TIMEOUT
+    assert pkv.device_status() == (0, 0)
+    _full_small_check(spec, pl)
+
+
+def test_cuda_graph_capture_of_a_step():
+    spec = SPECS["llama8b_layer_b8"]
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    _, _, _, ref = case.oracle()
+    d = case.device()
+    ws = torch.empty(pkv.workspace_bytes(8, 32, 8, 128), dtype=torch.uint8, device="cuda")
+    out = torch.empty(8, 32, 128, dtype=torch.float32, device="cuda")
+    slots = torch.empty(8, dtype=torch.int32, device="cuda")
+    # Warm-up outside the capture (loads the kernels, sets their attributes).
+    pkv.slot_mapping(d["tables"], d["ctx"], 16, pl.num_blocks, out=slots)
+    pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                               out=out, out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            pkv.slot_mapping(d["tables"], d["ctx"], 16, pl.num_blocks, out=slots)
+            d["pool"].append(0, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
+            pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                                       out=out, out_dtype=torch.float32, workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    check_output(out, ref, "graph replay")
+    g.replay()  # appending the same rows again is idempotent
+    torch.cuda.synchronize()
+    check_output(out, ref, "second replay")
