@@ -1,0 +1,472 @@
+"""Benchmark of one continuous-batching decode step over a paged KV cache.
+
+A step is the whole hot path over one batch: the newest-token slot mapping,
+then for every layer the KV append and the paged decode attention.  The
+default workload is the Llama-3-8B-shaped batch-32 step: 32 layers, 32
+sequences of 4096 tokens (the appended token included), 32 query / 8 KV
+heads, head_dim 128, bf16 K/V, 16-token blocks, a 16384-block pool per layer.
+
+Timed region: K graph replays of the captured step, bracketed by a barrier and
+a device synchronize, CUDA events on the replay stream, max over ranks.  One
+step reads 17.2 GB of K/V, far above the 129 MB L2, so no flush is needed.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host cores instead (bounded samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import SPECS, fill_pool_layer, make_placement, pool_layer_values, step_layer_values  # noqa: E402
+
+METRIC = "paged decode-attention KV GB/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNEL_SOURCES = ("decode_kernel.cuh", "decode_mma.cu", "decode_ffma.cu", "device_utils.cuh",
+                  "decode_plan.cu")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama8b_32l_b32", choices=sorted(SPECS))
+    p.add_argument("--kernel", default="auto", choices=["auto", "mma", "ffma"])
+    p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, use_cuda):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if use_cuda else "gloo")
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_slots_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split())
+        if f.get("kernel") == kernel_name and f.get("workload") == workload and f.get("sources") == want:
+            return int(f["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms meanwhile."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- our arm
+class Step:
+    """Device state of the benchmark workload and one decode step through the library."""
+
+    def __init__(self, spec, kernel, device):
+        import paged_kv_cache_slots_gb300 as pkv
+        self.pkv = pkv
+        self.spec, self.kernel, self.dev = spec, kernel, device
+        self.pl = make_placement(spec)
+        s, pl = spec, self.pl
+        B = len(pl.context_lens)
+        self.B = B
+        self.pool = pkv.KVPool(s.num_layers, pl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim,
+                               s.torch_dtype, device=device)
+        self.layers = [self.pool.layer(l) for l in range(s.num_layers)]
+        for l, (kc, vc) in enumerate(self.layers):
+            fill_pool_layer(s, l, kc, vc)
+        self.q = torch.empty((s.num_layers, B, s.num_q_heads, s.head_dim), dtype=s.torch_dtype, device=device)
+        self.kn = torch.empty((s.num_layers, B, s.num_kv_heads, s.head_dim), dtype=s.torch_dtype, device=device)
+        self.vn = torch.empty_like(self.kn)
+        for l in range(s.num_layers):
+            q, kn, vn = step_layer_values(s, B, l, device)
+            self.q[l].copy_(q)
+            self.kn[l].copy_(kn)
+            self.vn[l].copy_(vn)
+        self.tables = torch.from_numpy(pl.block_tables).to(device)
+        self.ctx = torch.from_numpy(pl.context_lens).to(device)
+        self.seq_ids = torch.from_numpy(np.where(pl.appends, np.arange(B), -1).astype(np.int32)).to(device)
+        self.slots = torch.empty(B, dtype=torch.int32, device=device)
+        self.out = torch.empty((s.num_layers, B, s.num_q_heads, s.head_dim), dtype=s.torch_dtype, device=device)
+        self.ws = torch.empty(pkv.workspace_bytes(B, s.num_q_heads, s.num_kv_heads, s.head_dim, device,
+                                                  kernel=kernel), dtype=torch.uint8, device=device)
+        self.launches_per_step = 1 + 3 * s.num_layers
+
+    def run(self, events=None):
+        s, pkv = self.spec, self.pkv
+        pkv.slot_mapping(self.tables, self.ctx, s.block_size, self.pl.num_blocks, out=self.slots)
+        for l, (kc, vc) in enumerate(self.layers):
+            self.pool.append(l, self.kn[l], self.vn[l], self.slots, seq_ids=self.seq_ids)
+            if events is not None:
+                events[l][0].record()
+            pkv.paged_decode_attention(self.q[l], kc, vc, self.tables, self.ctx, s.attn_scale,
+                                       out=self.out[l], workspace=self.ws, kernel=self.kernel)
+            if events is not None:
+                events[l][1].record()
+
+
+def bench_ours(args, world, rank, local):
+    import paged_kv_cache_slots_gb300 as pkv
+    from paged_kv_cache_slots_gb300 import roofline
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, True)
+    spec = SPECS[args.workload]
+    step = Step(spec, args.kernel, dev)
+    pl = step.pl
+    B = step.B
+    bytes_layer = roofline.attention_bytes(pl.context_lens, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                                           spec.elem_bytes, spec.block_size, spec.elem_bytes,
+                                           int(pl.appends.sum()))
+    kv_bytes_step = bytes_layer.kv * spec.num_layers
+
+    # Warm-up (eager), then parity spot check of the last layer against nothing
+    # but the device status word (the parity tests cover correctness).
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    st, flags = pkv.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x} after warm-up")
+
+    # Capture one step in a CUDA graph.
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step.run()
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    # Timed region: K replays.
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    ms_step = ms_total / args.steps
+    clock = clocks.summary()
+    st, flags = pkv.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x} after the timed region")
+
+    # Dominant kernel: per-launch duration of the attention call (partial +
+    # reduce kernels) from events on its stream, eager, over a few steps.
+    n_steps_ev = 5
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(spec.num_layers)] for _ in range(n_steps_ev)]
+    torch.cuda.synchronize()
+    for i in range(n_steps_ev):
+        step.run(events=evs[i])
+    torch.cuda.synchronize()
+    launch_ms = statistics.mean(a.elapsed_time(b) for e in evs for a, b in e)
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_layer.attention / (launch_ms * 1e-3) / 1e9
+    kernel_name = "paged_decode_partial_kernel<MmaPolicy>" if step.kernel != "ffma" else \
+        "paged_decode_partial_kernel<FfmaPolicy>"
+    traffic = recorded_traffic(kernel_name, spec.name)
+
+    # End to end through the public API with host buffers (pinned), copies timed.
+    h_q = step.q.cpu().pin_memory()
+    h_kn = step.kn.cpu().pin_memory()
+    h_vn = step.vn.cpu().pin_memory()
+    h_tab = torch.from_numpy(pl.block_tables).pin_memory()
+    h_ctx = torch.from_numpy(pl.context_lens).pin_memory()
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_tab, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        step.q.copy_(h_q, non_blocking=True)
+        step.kn.copy_(h_kn, non_blocking=True)
+        step.vn.copy_(h_vn, non_blocking=True)
+        step.tables.copy_(h_tab, non_blocking=True)
+        step.ctx.copy_(h_ctx, non_blocking=True)
+        step.run()
+        h_out.copy_(step.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.e2e_steps
+
+    kv_total = sum_over_ranks(kv_bytes_step, world, dev)
+    value = kv_total / (ms_step * 1e-3) / 1e9
+    e2e_value = kv_total / (e2e_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "accumulate": "f32",
+        "data": "synthetic (seeded N(0,1) q/K/V, random block placement)",
+        "config": {"workload": f"{spec.name}: {spec.num_layers} layers x {B} seqs x "
+                               f"{int(pl.context_lens.max())} ctx (appended token included), "
+                               f"{spec.num_q_heads}q/{spec.num_kv_heads}kv heads, D{spec.head_dim}, "
+                               f"{spec.dtype}, block {spec.block_size}, {pl.num_blocks}-block pool",
+                   "num_layers": spec.num_layers, "num_seqs": B, "context_tokens": int(pl.context_lens.sum()),
+                   "kv_bytes_per_step": kv_bytes_step, "kernel": step.kernel,
+                   "timing": "CUDA-graph replay of the whole step, CUDA events on the replay stream",
+                   "l2": "no flush: each step reads %.1f GB of K/V (> 129 MB L2)" % (kv_bytes_step / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "decode_tokens_per_s": round(sum_over_ranks(B, world, dev) / (ms_step * 1e-3), 1),
+        "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "frac_of_measured_hbm": round(value / world / peak, 4),
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "python binding -> C ABI, pinned host buffers, copies in the timed region"},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": kernel_name + " + paged_decode_reduce_kernel",
+                     "algorithmic_bytes_per_launch": bytes_layer.attention,
+                     "launch_ms": round(launch_ms, 5), "peak_source": f"{peak_kind} hbm_gbs"},
+        "clocks": clock,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(spec, pl, args.cpu_seconds, step)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------- oracle arm
+def oracle_sample(spec, pl, layer_pools=None, device="cpu"):
+    """Host inputs of one layer's sampled step for the oracle (compact pool)."""
+    if layer_pools is None:
+        kc, vc = pool_layer_values(spec, pl.num_blocks, 0, device)
+    else:
+        kc, vc = layer_pools
+    rows = pl.block_tables
+    used = np.unique(rows[rows >= 0])
+    remap = np.full(pl.num_blocks, -1, dtype=np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    tabs = np.where(rows >= 0, remap[np.maximum(rows, 0)], -1).astype(np.int32)
+    idx = torch.from_numpy(used.astype(np.int64)).to(kc.device)
+    return kc[idx].cpu(), vc[idx].cpu(), tabs
+
+
+def cpu_baseline(spec, pl, seconds, step=None):
+    """The oracle (as it stands) on layer 0 of the workload, repeated for ~`seconds`."""
+    import oracle
+    from paged_kv_cache_slots_gb300 import roofline
+
+    B = len(pl.context_lens)
+    if step is not None:
+        kc, vc, tabs = oracle_sample(spec, pl, step.layers[0])
+        q = step.q[0].cpu()
+    else:
+        kc, vc, tabs = oracle_sample(spec, pl)
+        q, _, _ = step_layer_values(spec, B, 0, "cpu")
+    cores = oracle.num_cores()
+    b = roofline.attention_bytes(pl.context_lens, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                                 spec.elem_bytes, spec.block_size, spec.elem_bytes, 0)
+    # One sequence at a time, until the time budget is used (at least one).
+    t0 = time.perf_counter()
+    done_bytes = 0
+    n = 0
+    while True:
+        s = n % B
+        oracle.paged_decode(q[s:s + 1], kc, vc, tabs[s:s + 1], pl.context_lens[s:s + 1], spec.attn_scale,
+                            nthreads=cores)
+        done_bytes += int(pl.context_lens[s]) * spec.num_kv_heads * spec.head_dim * 2 * spec.elem_bytes
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"layer 0, {n} sequence passes (all {spec.num_q_heads} query heads each), "
+                      f"{done_bytes / 1e9:.2f} GB of K/V in {dt:.1f} s",
+            "full_layer_kv_bytes": b.kv}
+
+
+def bench_reference(args, world, rank):
+    """The oracle as the reference arm: host cores, bounded samples of the workload."""
+    import oracle
+
+    if rank != 0:
+        return
+    spec = SPECS[args.workload]
+    pl = make_placement(spec)
+    kc, vc, tabs = oracle_sample(spec, pl)
+    B = len(pl.context_lens)
+    q, _, _ = step_layer_values(spec, B, 0, "cpu")
+    cores = oracle.num_cores()
+
+    def one(i):
+        s = i % B
+        oracle.paged_decode(q[s:s + 1], kc, vc, tabs[s:s + 1], pl.context_lens[s:s + 1], spec.attn_scale,
+                            nthreads=cores)
+        return int(pl.context_lens[s]) * spec.num_kv_heads * spec.head_dim * 2 * spec.elem_bytes
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    done = sum(one(i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/K/V, random block placement)",
+        "config": {"workload": f"{spec.name} (oracle arm: each step is one sequence of layer 0, "
+                               f"all {spec.num_q_heads} query heads)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps x one sequence of layer 0 of {spec.name}"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        bench_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    bench_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

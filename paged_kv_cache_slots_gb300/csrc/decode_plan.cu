@@ -53,13 +53,19 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeAr
     const int ca = cta_of_tile(pa, W, a.num_ctas);
     const int cb = cta_of_tile(pa + nb - 1, W, a.num_ctas);
     if (ca == cb) return;
+    // CTAs between ca and cb whose tile range is empty (more CTAs than tiles)
+    // wrote nothing for this pair and are skipped.
+    const int64_t P = a.num_ctas;
     for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
         const int g = idx / D, d = idx - g * D;
         float M = -INFINITY;
-        for (int c = ca; c <= cb; ++c)
+        for (int c = ca; c <= cb; ++c) {
+            if (c * W / P == (c + 1) * W / P) continue;
             M = fmaxf(M, a.part_ml[((static_cast<int64_t>(c) + pair) * G + g) * 2]);
+        }
         float Lsum = 0.f, O = 0.f;
         for (int c = ca; c <= cb; ++c) {
+            if (c * W / P == (c + 1) * W / P) continue;
             const int64_t sl = (static_cast<int64_t>(c) + pair) * G + g;
             const float wgt = fast_exp2(a.part_ml[sl * 2] - M);
             Lsum += wgt * a.part_ml[sl * 2 + 1];

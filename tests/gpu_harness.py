@@ -41,6 +41,20 @@ def check_output(out: torch.Tensor, ref: np.ndarray, what: str):
     return float(err.max()) if err.size else 0.0
 
 
+def attend(q, kc, vc, tables, ctx, scale, out_dtype=None, **opts):
+    """paged_decode_attention with a NaN-filled output and an 0xFF-filled
+    workspace, so that an output the kernels fail to write, or a partial they
+    read without having written it, cannot pass unnoticed."""
+    B, Hq, D = q.shape
+    out_dtype = out_dtype or q.dtype
+    out = torch.full((B, Hq, D), float("nan"), dtype=out_dtype, device=q.device)
+    n = pkv.workspace_bytes(B, Hq, kc.shape[1], D, q.device,
+                            **{k: v for k, v in opts.items() if k != "test_stall"})
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=q.device)
+    return pkv.paged_decode_attention(q, kc, vc, tables, ctx, scale, out=out, out_dtype=out_dtype,
+                                      workspace=ws, **opts)
+
+
 def newest_slot_masks(placement):
     """seq_ids passed to the append: -1 marks a sequence that writes nothing."""
     return np.where(placement.appends, np.arange(len(placement.appends)), -1).astype(np.int32)
@@ -82,8 +96,8 @@ def run_step(d, spec, num_blocks, layer=0, out_dtype=None, **opts):
     """Slot mapping, append and attention of one layer through the library."""
     slots = pkv.slot_mapping(d["tables"], d["ctx"], spec.block_size, num_blocks)
     d["pool"].append(layer, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
-    out = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
-                                     spec.attn_scale, out_dtype=out_dtype, **opts)
+    out = attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                 out_dtype=out_dtype, **opts)
     return slots, out
 
 
@@ -124,9 +138,8 @@ class LargeCase:
         k_pre, v_pre = kc[used_t].cpu(), vc[used_t].cpu()  # the oracle's pool: pre-append
         slots = pkv.slot_mapping(self.tables, self.ctx, s.block_size, pl.num_blocks)
         self.pool.append(layer, kn, vn, slots, seq_ids=self.seq_ids)
-        out32 = pkv.paged_decode_attention(q, kc, vc, self.tables, self.ctx, s.attn_scale,
-                                           out_dtype=torch.float32, **opts)
-        outq = pkv.paged_decode_attention(q, kc, vc, self.tables, self.ctx, s.attn_scale, **opts)
+        out32 = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, out_dtype=torch.float32, **opts)
+        outq = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, **opts)
         st, flags = pkv.device_status()
         assert st == 0 and flags == 0, f"device status {st} flags {flags:#x}"
         # Oracle on the sampled sequences, over the compact pool.

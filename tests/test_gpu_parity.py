@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import paged_kv_cache_slots_gb300 as pkv
-from gpu_harness import (LargeCase, SmallCase, bits, check_output, run_step, sample_sequences)
+from gpu_harness import (LargeCase, SmallCase, attend, bits, check_output, run_step, sample_sequences)
 from workloads import SPECS, make_placement, small_spec
 
 pytestmark = pytest.mark.gpu
@@ -36,7 +36,7 @@ def _full_small_check(spec, placement=None, kernels=("auto",), **opts):
     for kernel in kernels:
         d = case.device()
         slots, out = run_step(d, spec, pl.num_blocks, out_dtype=torch.float32, kernel=kernel, **opts)
-        outq = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
+        outq = attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
                                           spec.attn_scale, kernel=kernel, **opts)
         st, flags = pkv.device_status()
         assert st == 0 and flags == 0, (st, flags)
@@ -133,7 +133,7 @@ def test_split_and_warp_counts_agree(kernel):
     d["pool"].append(0, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
     outs = []
     for num_ctas, warps in [(0, 0), (1, 8), (2, 1), (7, 3), (64, 8), (1000, 15), (152, 4)]:
-        out = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
+        out = attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
                                          spec.attn_scale, out_dtype=torch.float32, kernel=kernel,
                                          num_ctas=num_ctas, consumer_warps=warps)
         check_output(out, ref, f"num_ctas={num_ctas} warps={warps}")
@@ -150,7 +150,7 @@ def test_block_relabelling_is_bitwise_invariant(kernel):
     pl = make_placement(spec)
     case = SmallCase(spec, pl)
     d = case.device()
-    base = pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+    base = attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
                                       kernel=kernel)
     perm = torch.randperm(pl.num_blocks, generator=torch.Generator().manual_seed(3))
     kc2, vc2 = torch.empty_like(d["kc"]), torch.empty_like(d["vc"])
@@ -158,7 +158,7 @@ def test_block_relabelling_is_bitwise_invariant(kernel):
     vc2[perm.cuda()] = d["vc"]
     t = torch.from_numpy(pl.block_tables).long()
     t2 = torch.where(t >= 0, perm[t.clamp(min=0)], torch.full_like(t, -1)).int().cuda()
-    out = pkv.paged_decode_attention(d["q"], kc2, vc2, t2, d["ctx"], spec.attn_scale, kernel=kernel)
+    out = attend(d["q"], kc2, vc2, t2, d["ctx"], spec.attn_scale, kernel=kernel)
     assert torch.equal(bits(out), bits(base))
 
 
@@ -173,7 +173,7 @@ def test_equal_heads_and_shared_tables(kernel):
     q = d["q"].clone()
     q[:, 1] = q[:, 0]
     q[1] = q[0]
-    out = pkv.paged_decode_attention(q, d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+    out = attend(q, d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
                                      kernel=kernel)
     assert torch.equal(bits(out[:, 1]), bits(out[:, 0]))
     assert torch.equal(bits(out[1]), bits(out[0]))
@@ -208,7 +208,7 @@ def test_device_checks_flag_and_continue():
     assert pkv.device_status() == (0, 0)
     bad = d["tables"].clone()
     bad[0, 1] = pl.num_blocks + 5  # outside the pool
-    pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], bad, d["ctx"], spec.attn_scale)
+    attend(d["q"], d["kc"], d["vc"], bad, d["ctx"], spec.attn_scale)
     st, flags = pkv.device_status()
     assert st == 7 and flags & pkv.FLAG_BAD_BLOCK_ID
     assert pkv.device_status() == (0, 0)  # read and cleared
@@ -219,7 +219,7 @@ def test_device_checks_flag_and_continue():
     assert st == 7 and flags == pkv.FLAG_BAD_SLOT
     assert torch.equal(bits(before), bits(d["kc"]))  # nothing written
     long_ctx = torch.tensor([40, 10_000], dtype=torch.int32, device="cuda")
-    pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], long_ctx, spec.attn_scale)
+    attend(d["q"], d["kc"], d["vc"], d["tables"], long_ctx, spec.attn_scale)
     st, flags = pkv.device_status()
     assert st == 7 and flags & pkv.FLAG_BAD_CONTEXT
     # The context stays usable: a clean call afterwards is still exact.
@@ -233,7 +233,7 @@ def test_bounded_wait_times_out_cleanly():
     pl = make_placement(spec)
     case = SmallCase(spec, pl)
     d = case.device()
-    pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+    attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
                                num_ctas=1, test_stall=True)
     st, flags = pkv.device_status()
     assert st == 8 and flags & pkv.FLAG_TIMEOUT
@@ -247,8 +247,8 @@ def test_cuda_graph_capture_of_a_step():
     case = SmallCase(spec, pl)
     _, _, _, ref = case.oracle()
     d = case.device()
-    ws = torch.empty(pkv.workspace_bytes(8, 32, 8, 128), dtype=torch.uint8, device="cuda")
-    out = torch.empty(8, 32, 128, dtype=torch.float32, device="cuda")
+    ws = torch.full((pkv.workspace_bytes(8, 32, 8, 128),), 0xFF, dtype=torch.uint8, device="cuda")
+    out = torch.full((8, 32, 128), float("nan"), dtype=torch.float32, device="cuda")
     slots = torch.empty(8, dtype=torch.int32, device="cuda")
     # Warm-up outside the capture (loads the kernels, sets their attributes).
     pkv.slot_mapping(d["tables"], d["ctx"], 16, pl.num_blocks, out=slots)
