@@ -16,6 +16,7 @@ on the host cores instead (bounded samples of the same workload).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -51,6 +52,13 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llama8b_32l_b32", choices=sorted(SPECS))
     p.add_argument("--kernel", default="auto", choices=["auto", "mma", "ffma"])
+    p.add_argument("--consumer-warps", type=int, default=0, help="0: library default")
+    p.add_argument("--ctas-per-sm", type=int, default=0, help="0: library default")
+    p.add_argument("--heads-per-stage", type=int, default=0, help="0: library default")
+    p.add_argument("--separate-reduce", action="store_true")
+    p.add_argument("--no-pdl", action="store_true")
+    p.add_argument("--layers", type=int, default=0,
+                   help="profiling only: run the first N layers (the JSON line then names N)")
     p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -181,10 +189,11 @@ class ClockSampler:
 class Step:
     """Device state of the benchmark workload and one decode step through the library."""
 
-    def __init__(self, spec, kernel, device):
+    def __init__(self, spec, kernel, device, **opts):
         import paged_kv_cache_slots_gb300 as pkv
         self.pkv = pkv
         self.spec, self.kernel, self.dev = spec, kernel, device
+        self.opts = dict(kernel=kernel, **opts)
         self.pl = make_placement(spec)
         s, pl = spec, self.pl
         B = len(pl.context_lens)
@@ -207,9 +216,8 @@ class Step:
         self.seq_ids = torch.from_numpy(np.where(pl.appends, np.arange(B), -1).astype(np.int32)).to(device)
         self.slots = torch.empty(B, dtype=torch.int32, device=device)
         self.out = torch.empty((s.num_layers, B, s.num_q_heads, s.head_dim), dtype=s.torch_dtype, device=device)
-        self.ws = torch.empty(pkv.workspace_bytes(B, s.num_q_heads, s.num_kv_heads, s.head_dim, device,
-                                                  kernel=kernel), dtype=torch.uint8, device=device)
-        self.launches_per_step = 1 + 3 * s.num_layers
+        self.ws = pkv.make_workspace(B, s.num_q_heads, s.num_kv_heads, s.head_dim, device, **self.opts)
+        self.launches_per_step = 1 + (3 if self.opts.get("separate_reduce") else 2) * s.num_layers
 
     def run(self, events=None):
         s, pkv = self.spec, self.pkv
@@ -219,7 +227,7 @@ class Step:
             if events is not None:
                 events[l][0].record()
             pkv.paged_decode_attention(self.q[l], kc, vc, self.tables, self.ctx, s.attn_scale,
-                                       out=self.out[l], workspace=self.ws, kernel=self.kernel)
+                                       out=self.out[l], workspace=self.ws, **self.opts)
             if events is not None:
                 events[l][1].record()
 
@@ -232,7 +240,11 @@ def bench_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     init_dist(world, True)
     spec = SPECS[args.workload]
-    step = Step(spec, args.kernel, dev)
+    if args.layers:
+        spec = dataclasses.replace(spec, num_layers=args.layers)
+    step = Step(spec, args.kernel, dev, consumer_warps=args.consumer_warps, ctas_per_sm=args.ctas_per_sm,
+                heads_per_stage=args.heads_per_stage, separate_reduce=args.separate_reduce,
+                pdl=not args.no_pdl)
     pl = step.pl
     B = step.B
     bytes_layer = roofline.attention_bytes(pl.context_lens, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
@@ -355,7 +367,8 @@ def bench_ours(args, world, rank, local):
         "gpu_launches": step.launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": kernel_name + " + paged_decode_reduce_kernel",
+                     "kernel": kernel_name + (" + paged_decode_reduce_kernel" if args.separate_reduce
+                                              else " (cross-CTA merge fused)"),
                      "algorithmic_bytes_per_launch": bytes_layer.attention,
                      "launch_ms": round(launch_ms, 5), "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clock,

@@ -78,6 +78,7 @@ typedef enum {
 #define KV_FLAG_BAD_SLOT       0x2u /* an append slot >= num_blocks*block_size */
 #define KV_FLAG_BAD_CONTEXT    0x4u /* context_lens[s] < 0 or > max_blocks_per_seq*block_size */
 #define KV_FLAG_TIMEOUT        0x8u /* a kernel gave up a bounded wait */
+#define KV_FLAG_BAD_PLAN       0x10u /* a launch plan the kernel refuses (never set by this library's own planning) */
 
 /* Human-readable name of a status code (static string). */
 const char* kv_status_string(kv_status_t status);
@@ -160,15 +161,23 @@ typedef enum {
 } kv_kernel_t;
 
 typedef struct {
-    int num_ctas;       /* persistent grid size; 0 = SM count x ctas_per_sm */
-    int ctas_per_sm;    /* 0 = 1 */
-    int consumer_warps; /* compute warps per CTA, 1..15; 0 = 8 */
+    int num_ctas;        /* persistent grid size; 0 = SM count x ctas_per_sm */
+    int ctas_per_sm;     /* 0 = 1 */
+    int consumer_warps;  /* compute warps per CTA, 1..15; 0 = about 8 */
     kv_kernel_t kernel;
-    int test_stall;     /* testing only, 0 in normal use: when non-zero, the
-                           producer of CTA 0 stops after one tile so that a
-                           consumer's bounded wait (about 2 s) runs out; the
-                           call then reports KV_ERR_DEVICE_TIMEOUT through
-                           kv_device_status and the output is undefined */
+    int heads_per_stage; /* KV heads whose K/V rows of one block form one pipeline
+                            stage; must divide num_kv_heads; 0 = the largest
+                            divisor whose K slab of a block fits 32 KiB */
+    int separate_reduce; /* 1: merge the partials of split sequences in a second
+                            kernel; 0: the last CTA to finish a sequence merges
+                            them inside the attention kernel */
+    int no_pdl;          /* 1: plain launches; 0: programmatic dependent launch
+                            (a kernel's prologue overlaps the previous kernel) */
+    int test_stall;      /* testing only, 0 in normal use: when non-zero, the
+                            producer of CTA 0 stops after one stage so that a
+                            consumer's bounded wait (about 2 s) runs out; the
+                            call then reports KV_ERR_DEVICE_TIMEOUT through
+                            kv_device_status and the output is undefined */
 } kv_decode_options_t;
 
 /* Workspace bytes paged_decode_attention needs for these sizes on `device`
@@ -176,6 +185,14 @@ typedef struct {
 kv_status_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                          int head_dim, int device,
                                          const kv_decode_options_t* opts, size_t* bytes_out);
+
+/* Zero the part of a workspace that must start at zero (the per-(sequence,
+ * KV head) merge counters at its start), asynchronously on `stream`.  Call it
+ * once after allocating a workspace (or zero the whole buffer); every
+ * completed call of paged_decode_attention leaves the counters zero again.
+ * After a call that reported KV_ERR_DEVICE_TIMEOUT, call it again. */
+kv_status_t paged_decode_workspace_init(void* workspace, size_t workspace_bytes, int num_seqs,
+                                        int num_kv_heads, void* stream);
 
 /* Single-query attention over the paged cache, for every sequence s and query
  * head g (KV head h = g / (num_q_heads / num_kv_heads)):
@@ -192,15 +209,18 @@ kv_status_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_
  *   out          device [num_seqs][num_q_heads][head_dim], out_dtype
  *                (KV_F32, or the same dtype as q)
  *   workspace    device scratch of workspace_bytes >= the size given by
- *                paged_decode_workspace_bytes for the same sizes and options;
- *                no initialisation needed; not to be shared by two calls in
- *                flight at once
+ *                paged_decode_workspace_bytes for the same sizes and options,
+ *                256-byte aligned, initialised once with
+ *                paged_decode_workspace_init (or zero-filled); not to be
+ *                shared by two calls in flight at once
  * Supported: head_dim 64 or 128, block_size 8..256 a multiple of 8,
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}; dtype f32, f16 or bf16.
- * The work of all sequences is split evenly over a persistent grid; each CTA
- * writes an fp32 partial (unnormalised output, running max, running sum) for
- * every sequence/KV head it only partly covers, and a second kernel merges
- * the partials (log-sum-exp).  Accumulation is fp32 throughout. */
+ * The work of all sequences -- (sequence, group of KV heads, block) items --
+ * is split evenly over a persistent grid; each CTA writes an fp32 partial
+ * (unnormalised output, running max, running sum) for every sequence/KV head
+ * it only partly covers, and the partials are merged (log-sum-exp) by the
+ * last CTA to finish that sequence or by a second kernel
+ * (separate_reduce).  Accumulation is fp32 throughout. */
 kv_status_t paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                                    int num_blocks, const int32_t* block_tables,
                                    int max_blocks_per_seq, const int32_t* context_lens,

@@ -18,7 +18,8 @@ from . import build as _build
 
 __all__ = [
     "KVError", "KVPool", "BlockAllocator", "kv_pool_bytes", "slot_mapping", "workspace_bytes",
-    "paged_decode_attention", "device_status", "library_path", "load_library",
+    "paged_decode_attention", "device_status", "library_path", "load_library", "workspace_init",
+    "make_workspace",
 ]
 
 KV_F32, KV_F16, KV_BF16 = 0, 1, 2
@@ -49,7 +50,8 @@ class _PoolConfig(ctypes.Structure):
 class _DecodeOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("consumer_warps", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("test_stall", ctypes.c_int)]
+                ("heads_per_stage", ctypes.c_int), ("separate_reduce", ctypes.c_int),
+                ("no_pdl", ctypes.c_int), ("test_stall", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -73,6 +75,7 @@ def _declare(lib):
                                              ctypes.POINTER(SZ)]),
         "paged_decode_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P,
                                        I, P, SZ, ctypes.POINTER(_DecodeOptions), P]),
+        "paged_decode_workspace_init": (I, [P, SZ, I, I, P]),
         "kv_device_status": (I, [I, P, U32P]),
         "kv_allocator_create": (I, [I, I, I, ctypes.POINTER(P)]),
         "kv_allocator_destroy": (None, [P]),
@@ -217,9 +220,24 @@ def slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor, block_s
     return out
 
 
-def _options(num_ctas=0, ctas_per_sm=0, consumer_warps=0, kernel="auto",
-             test_stall=False) -> _DecodeOptions:
-    return _DecodeOptions(num_ctas, ctas_per_sm, consumer_warps, KERNELS[kernel], int(test_stall))
+def _options(num_ctas=0, ctas_per_sm=0, consumer_warps=0, kernel="auto", heads_per_stage=0,
+             separate_reduce=False, pdl=True, test_stall=False) -> _DecodeOptions:
+    return _DecodeOptions(num_ctas, ctas_per_sm, consumer_warps, KERNELS[kernel], heads_per_stage,
+                          int(separate_reduce), int(not pdl), int(test_stall))
+
+
+def workspace_init(workspace: torch.Tensor, num_seqs: int, num_kv_heads: int, stream=None):
+    """Zero the merge counters at the start of a workspace (once after allocation)."""
+    lib = load_library()
+    _check(lib.paged_decode_workspace_init(_ptr(workspace), workspace.numel(), num_seqs, num_kv_heads,
+                                           _stream(workspace, stream)), lib)
+
+
+def make_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, device=None, **opts) -> torch.Tensor:
+    """A zero-filled workspace for paged_decode_attention with these sizes and options."""
+    dev = torch.device(device if device is not None else "cuda")
+    n = workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, dev, **opts)
+    return torch.zeros(n, dtype=torch.uint8, device=dev)
 
 
 def workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, device=None, **opts) -> int:
@@ -255,8 +273,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     _need(out.dtype == out_dtype and tuple(out.shape) == (B, Hq, D) and out.is_contiguous(), "out")
     o = _options(**opts)
     if workspace is None:
-        workspace = torch.empty(workspace_bytes(B, Hq, Hkv, D, q.device, **opts), dtype=torch.uint8,
-                                device=q.device)
+        workspace = make_workspace(B, Hq, Hkv, D, q.device, **opts)
     _check(lib.paged_decode_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), B, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale), _ptr(out),

@@ -12,6 +12,8 @@ namespace pkv {
 // 16-byte vectors: lanes [0, n) copy the K row, lanes [n, 2n) the V row
 // (n = row bytes / 16; head_dim * elem is a multiple of 16 by validation).
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
+    pdl_allow_next();
+    pdl_wait();
     const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp >= a.n_tokens * a.num_kv_heads) return;
@@ -43,6 +45,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
 }
 
 __global__ void __launch_bounds__(256) kv_slot_mapping_kernel(const SlotArgs a) {
+    pdl_allow_next();
+    pdl_wait();
     const int s = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
     if (s >= a.num_seqs) return;
     const int ctx = a.context_lens[s];
@@ -70,15 +74,15 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     if (warps == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (warps * 32 + threads - 1) / threads;
-    kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+                         stream, a.pdl != 0, a);
 }
 
 cudaError_t launch_slot_mapping(const SlotArgs& a, cudaStream_t stream) {
     if (a.num_seqs == 0) return cudaSuccess;
     const int threads = 256;
-    kv_slot_mapping_kernel<<<(a.num_seqs + threads - 1) / threads, threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kv_slot_mapping_kernel, dim3((a.num_seqs + threads - 1) / threads),
+                         dim3(threads), 0, stream, a.pdl != 0, a);
 }
 
 }  // namespace pkv

@@ -100,11 +100,14 @@ struct FfmaPolicy {
         }
     }
 
-    __device__ __forceinline__ void tile(State& st, const DecodeArgs&, const uint8_t* kt,
-                                         const uint8_t* vt, int n_valid, int, float* sc) {
+    // One head's part of a stage: kt/vt point at the stage's K/V, laid out as
+    // [Hc][bs][D]; this warp's head is hw.
+    __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, const uint8_t* kt,
+                                         const uint8_t* vt, int hw, int n_valid, int, float* sc) {
         const int lane = threadIdx.x & 31;
-        const T* K = reinterpret_cast<const T*>(kt) + lane * VD;
-        const T* V = reinterpret_cast<const T*>(vt) + lane * VD;
+        const int64_t head_off = static_cast<int64_t>(hw) * a.block_size * D;
+        const T* K = reinterpret_cast<const T*>(kt) + head_off + lane * VD;
+        const T* V = reinterpret_cast<const T*>(vt) + head_off + lane * VD;
         // Scores (base-2 units) of every valid token, into scratch[t][g].
         for (int t = 0; t < n_valid; ++t) {
             float k[VD];
@@ -166,17 +169,40 @@ struct FfmaPolicy {
         __syncwarp();
     }
 
-    // Write this warp's state to mw[g][0..D) (O), mw[g][D] (m), mw[g][D+1] (l).
-    __device__ __forceinline__ void publish(const State& st, const DecodeArgs&, float* mw, int) {
+    // O (unnormalised) to o[g*os + d], (max, sum) to ml[g*ms], ml[g*ms + 1].
+    __device__ __forceinline__ void emit(const State& st, float* o, int os, float* ml, int ms) const {
         const int lane = threadIdx.x & 31;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
 #pragma unroll
-            for (int i = 0; i < VD; ++i) mw[g * (D + 2) + lane * VD + i] = st.o[g][i];
+            for (int i = 0; i < VD; ++i) o[g * os + lane * VD + i] = st.o[g][i];
             if (lane == 0) {
-                mw[g * (D + 2) + D] = st.m[g];
-                mw[g * (D + 2) + D + 1] = st.l[g];
+                ml[g * ms] = st.m[g];
+                ml[g * ms + 1] = st.l[g];
             }
+        }
+    }
+
+    __device__ __forceinline__ void write_state(const State& st, const DecodeArgs&, float* dst,
+                                                int stride, int) const {
+        emit(st, dst, stride, dst + D, stride);
+    }
+
+    __device__ __forceinline__ void write_partial(const State& st, const DecodeArgs&, float* o,
+                                                  float* ml, int) const {
+        emit(st, o, D, ml, 2);
+    }
+
+    // out[s][h*G + g][d] = O / l in the output type.
+    __device__ __forceinline__ void write_final(const State& st, const DecodeArgs& a, int s, int h,
+                                                int) const {
+        const int lane = threadIdx.x & 31;
+        const int64_t base = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D + lane * VD;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float inv = 1.f / st.l[g];
+#pragma unroll
+            for (int i = 0; i < VD; ++i) store_out(a.out, base + g * D + i, st.o[g][i] * inv, a.out_dtype);
         }
     }
 };

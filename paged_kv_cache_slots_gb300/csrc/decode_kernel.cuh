@@ -4,25 +4,31 @@
 // "Batching and Scheduling", Example 1): for every sequence s and query head
 // g, softmax over the sequence's cached tokens of scale * q.k, applied to V,
 // with K/V read through the block table.  Query heads h*G .. h*G+G-1 share KV
-// head h, and one CTA reads each (block, kv head) tile from HBM once for the
-// whole group.
+// head h, and each (block, KV head) tile is read from HBM once for the whole
+// group.
 //
-// Work split.  The work space is every (sequence, kv head, logical block)
-// triple, in that order; W = sum_s Hkv * ceil(ctx_s / bs) tiles.  CTA c of P
-// owns tiles [c*W/P, (c+1)*W/P): the load is balanced to one tile whatever
-// the length mix.  A run of tiles of one (sequence, kv head) pair inside one
-// CTA is a segment.  A segment that covers its whole pair writes the final
-// output; otherwise it writes an fp32 partial (unnormalised O, running max,
-// running sum) to partial slot c + pair, which is unique because segments
-// sorted by position increase c + pair by at least one each step.  The
-// reduce kernel merges the partials of each split pair.
+// Work split.  A work item is (sequence, head chunk, logical block), where a
+// head chunk is Hc consecutive KV heads: their K rows of one block are
+// contiguous in the pool ([block][head][token][dim]), so an item is one
+// pipeline stage filled by two contiguous copies (K, V) of Hc*bs*D elements.
+// Items are ordered sequence-major; W = chunks * sum_s ceil(ctx_s / bs).
+// CTA c of P owns items [c*W/P, (c+1)*W/P): every CTA streams the same number
+// of items (to within one) whatever the length mix.  The run of one (sequence,
+// head chunk) pair inside one CTA is a segment.  A segment covering its whole
+// pair writes the final output; otherwise it writes fp32 partials
+// (unnormalised O, running max, running sum) to slot c + pair, unique because
+// segments sorted by position increase c + pair by at least one each step.
+// The partials of a split pair are merged (log-sum-exp, base 2) either by the
+// last warp to finish that (sequence, head) -- it counts arrivals on a
+// per-(sequence, head) counter that it resets to zero -- or by the separate
+// reduce kernel.
 //
-// Inside a CTA, warp 0 is the producer: it reads table entries 32 at a time
-// and streams each tile's K and V into a ring of shared-memory stages with
-// asynchronous bulk copies completing on mbarriers.  The other warps consume
-// tiles round-robin, each keeping an online-softmax state (scores in base-2
-// units) for the current segment, and merge their states through shared
-// memory at the end of the segment.
+// Inside a CTA, warp 0 produces: it resolves table entries 32 items at a time
+// and issues each item's two copies into a ring of shared-memory stages,
+// completing on mbarrier transaction counts.  Consumer warp w works on head
+// w % Hc of every chunk; R = consumer_warps / Hc warps per head take that
+// head's items round-robin and merge their states through shared memory at
+// the end of a segment (no merge when R == 1).
 #pragma once
 
 #include <atomic>
@@ -38,13 +44,13 @@ struct SmemLayout {
 };
 
 // Offsets from a 1024-byte aligned base; `total` includes the alignment slack.
-__host__ __device__ inline SmemLayout smem_layout(int stages, int tile_bytes, int num_seqs,
-                                                  int consumer_warps, int group, int head_dim,
-                                                  int block_size, bool scratch) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int stage_half_bytes, int num_seqs,
+                                                  int consumer_warps, int warps_per_head, int group,
+                                                  int head_dim, int block_size, bool scratch) {
     SmemLayout L;
     int o = 0;
     L.ring = o;
-    o += stages * 2 * tile_bytes;
+    o += stages * 2 * stage_half_bytes;
     L.full_bar = o;
     o += stages * 8;
     L.empty_bar = o;
@@ -56,16 +62,20 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int tile_bytes, in
     L.cum = o;
     o += ((num_seqs + 1) * 4 + 15) & ~15;
     L.merge = o;
-    o += consumer_warps * group * (head_dim + 2) * 4;
+    if (warps_per_head > 1) o += consumer_warps * group * (head_dim + 2) * 4;
     L.scratch = o;
     if (scratch) o += consumer_warps * ((block_size * group * 4 + 15) & ~15);
     L.total = o + 1024;
     return L;
 }
 
-// Tile index -> CTA that owns it: the c with floor(c*W/P) <= x < floor((c+1)*W/P).
-__host__ __device__ inline int cta_of_tile(int64_t x, int64_t W, int P) {
+// Item index -> CTA that owns it: the c with floor(c*W/P) <= x < floor((c+1)*W/P).
+__host__ __device__ inline int cta_of_item(int64_t x, int64_t W, int P) {
     return static_cast<int>(((x + 1) * P - 1) / W);
+}
+
+__host__ __device__ inline bool cta_is_empty(int64_t c, int64_t W, int64_t P) {
+    return c * W / P == (c + 1) * W / P;
 }
 
 // Largest s in [0, n) with cum[s] <= i (cum non-decreasing, cum[0] == 0).
@@ -91,8 +101,8 @@ __device__ __forceinline__ int clamp_context(const DecodeArgs& a, int s, bool fl
     return c;
 }
 
-// cum[s] = Hkv * sum_{s' < s} ceil(ctx_s' / bs); cum[num_seqs] = W.
-static __device__ void build_prefix(const DecodeArgs& a, int32_t* cum, int32_t* scan) {
+// cum[s] = chunks * sum_{s' < s} ceil(ctx_s' / bs); cum[num_seqs] = W.
+static __device__ void build_prefix(const DecodeArgs& a, int chunks, int32_t* cum, int32_t* scan) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     int carry = 0;
@@ -101,7 +111,7 @@ static __device__ void build_prefix(const DecodeArgs& a, int32_t* cum, int32_t* 
         int v = 0;
         if (s < a.num_seqs) {
             const int c = clamp_context(a, s, blockIdx.x == 0);
-            v = (c + a.block_size - 1) / a.block_size * a.num_kv_heads;
+            v = (c + a.block_size - 1) / a.block_size * chunks;
         }
         int x = v;
 #pragma unroll
@@ -131,71 +141,72 @@ static __device__ void build_prefix(const DecodeArgs& a, int32_t* cum, int32_t* 
 }
 
 // ------------------------------------------------------------------ producer
-// kTensor: tiles arrive through 2-D tensor maps with a 128-byte swizzle (box
-// of 64 elements x block_size rows, one box per 64-element half of the row);
-// otherwise as plain contiguous bulk copies.
+// kTensor: stages arrive through 2-D tensor maps with a 128-byte swizzle (box
+// of 64 elements x Hc*bs rows, one box per 64-element slice of the row);
+// otherwise as two plain contiguous bulk copies.
 template <bool kTensor>
-__device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                        const int32_t* cum, int start, int end, int tile_bytes,
+static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                        const int32_t* cum, int chunks, int start, int end, int half_bytes,
                         const CUtensorMap* tmk, const CUtensorMap* tmv, volatile int* abort) {
     const int lane = threadIdx.x & 31;
     const uint64_t policy = policy_evict_first();
-    const int stage_bytes = 2 * tile_bytes;
-    const int64_t row_elems = a.head_dim;
-    const int eb = dtype_bytes(a.dtype);
-    int issued = 0;  // tiles whose copies were issued (lane 0)
+    const int stage_bytes = 2 * half_bytes;
+    const int64_t row_bytes = static_cast<int64_t>(a.head_dim) * dtype_bytes(a.dtype);
+    int issued = 0;  // items whose copies were issued (lane 0)
+    int stage = 0, round = 0;
     bool ok = true;
     for (int base = start; base < end && ok; base += 32) {
         const int i = base + lane;
-        int64_t row = 0;  // first pool row of the tile: (blk * Hkv + h) * bs
+        int64_t row = 0;  // first pool row of the item: (blk * Hkv + hc * Hc) * bs
         if (i < end) {
             const int s = find_sequence(cum, a.num_seqs, i);
-            const int nb = (cum[s + 1] - cum[s]) / a.num_kv_heads;
+            const int nb = (cum[s + 1] - cum[s]) / chunks;
             const int r = i - cum[s];
-            const int h = r / nb;
-            const int j = r - h * nb;
+            const int hc = r / nb;
+            const int j = r - hc * nb;
             int blk = __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks + j);
             if (blk < 0 || blk >= a.num_blocks) {
                 raise_flag(a.status, kFlagBadBlock);
                 blk = 0;
             }
-            row = (static_cast<int64_t>(blk) * a.num_kv_heads + h) * a.block_size;
+            row = (static_cast<int64_t>(blk) * a.num_kv_heads + hc * a.heads_per_stage) * a.block_size;
         }
         const int n = min(32, end - base);
         for (int k = 0; k < n; ++k) {
             const int64_t rk = __shfl_sync(0xffffffffu, row, k);
             int good = 1;
             if (lane == 0) {
-                const int t = base + k - start;
-                const int stage = t % a.stages;
-                const int round = t / a.stages;
-                // Test-only stall: CTA 0 stops after its first tile, so that a
+                // Test-only stall: CTA 0 stops after its first item, so that a
                 // consumer's bounded wait for the second one runs out.
-                if (a.test_stall && blockIdx.x == 0 && t == 1) good = 0;
+                if (a.test_stall && blockIdx.x == 0 && base + k - start == 1) good = 0;
                 if (good && round > 0)
                     good = mbar_wait_bounded(&empty[stage], (round - 1) & 1, abort, a.status);
                 if (good) {
                     uint8_t* kd = ring + stage * stage_bytes;
-                    uint8_t* vd = kd + tile_bytes;
+                    uint8_t* vd = kd + half_bytes;
                     mbar_arrive_expect_tx(&full[stage], stage_bytes);
                     if constexpr (kTensor) {
-                        const int halves = a.head_dim / 64;
-                        const int half_bytes = tile_bytes / halves;
-                        for (int hf = 0; hf < halves; ++hf) {
-                            tensor_load_2d(kd + hf * half_bytes, tmk, hf * 64, static_cast<int>(rk),
+                        const int slices = a.head_dim / 64;
+                        const int slice_bytes = half_bytes / slices;
+                        for (int sl = 0; sl < slices; ++sl) {
+                            tensor_load_2d(kd + sl * slice_bytes, tmk, sl * 64, static_cast<int>(rk),
                                            &full[stage], policy);
-                            tensor_load_2d(vd + hf * half_bytes, tmv, hf * 64, static_cast<int>(rk),
+                            tensor_load_2d(vd + sl * slice_bytes, tmv, sl * 64, static_cast<int>(rk),
                                            &full[stage], policy);
                         }
                     } else {
-                        const int64_t off = rk * row_elems * eb;
-                        bulk_load(kd, static_cast<const char*>(a.k_cache) + off, tile_bytes,
+                        const int64_t off = rk * row_bytes;
+                        bulk_load(kd, static_cast<const char*>(a.k_cache) + off, half_bytes,
                                   &full[stage], policy);
-                        bulk_load(vd, static_cast<const char*>(a.v_cache) + off, tile_bytes,
+                        bulk_load(vd, static_cast<const char*>(a.v_cache) + off, half_bytes,
                                   &full[stage], policy);
                     }
                     ++issued;
                 }
+            }
+            if (++stage == a.stages) {
+                stage = 0;
+                ++round;
             }
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) {
@@ -222,19 +233,103 @@ __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* full, uint
     __syncwarp();
 }
 
+// ------------------------------------------------- merge of split pairs
+// Called by one warp per (sequence s, KV head h) after it wrote its partial
+// for slot c + pair.  Counts the arrival; the warp that arrives last merges
+// the nparts partials of (s, h) into the output and resets the counter.
+static __device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, int pair, int nparts,
+                              int ca, int cb, int64_t W, int G) {
+    const int lane = threadIdx.x & 31;
+    const int D = a.head_dim, Hc = a.heads_per_stage;
+    int32_t* counter = a.counters + static_cast<int64_t>(s) * a.num_kv_heads + h;
+    __threadfence();
+    __syncwarp();
+    int prev = 0;
+    if (lane == 0) prev = atomicAdd(counter, 1);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev != nparts - 1) return;
+    __threadfence();
+    const int64_t P = a.num_ctas;
+    for (int g = 0; g < G; ++g) {
+        float M = -INFINITY;
+        for (int c = ca; c <= cb; ++c) {
+            if (cta_is_empty(c, W, P)) continue;
+            const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g;
+            M = fmaxf(M, load_cg(a.part_ml + sl * 2));
+        }
+        float Lsum = 0.f;
+        for (int c = ca; c <= cb; ++c) {
+            if (cta_is_empty(c, W, P)) continue;
+            const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g;
+            Lsum += fast_exp2(load_cg(a.part_ml + sl * 2) - M) * load_cg(a.part_ml + sl * 2 + 1);
+        }
+        const float inv = 1.f / Lsum;
+        const int64_t o0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D;
+        for (int d = lane; d < D; d += 32) {
+            float O = 0.f;
+            for (int c = ca; c <= cb; ++c) {
+                if (cta_is_empty(c, W, P)) continue;
+                const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g;
+                O += fast_exp2(load_cg(a.part_ml + sl * 2) - M) * load_cg(a.part_o + sl * D + d);
+            }
+            store_out(a.out, o0 + d, O * inv, a.out_dtype);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) *counter = 0;
+}
+
+// Combine the R warps' states of head hw (shared memory, [warp][g][D+2]) and
+// write the final output (whole pair) or the CTA's partial.  One warp.
+static __device__ void combine_replicas(const DecodeArgs& a, const float* merge, int hw, int Hc, int R,
+                                 int G, bool whole, int s, int h, float* part_o, float* part_ml) {
+    const int lane = threadIdx.x & 31;
+    const int D = a.head_dim;
+    for (int g = 0; g < G; ++g) {
+        float M = -INFINITY;
+        for (int r = 0; r < R; ++r) M = fmaxf(M, merge[((hw + r * Hc) * G + g) * (D + 2) + D]);
+        float Lsum = 0.f;
+        for (int r = 0; r < R; ++r) {
+            const float* mr = merge + ((hw + r * Hc) * G + g) * (D + 2);
+            Lsum += fast_exp2(mr[D] - M) * mr[D + 1];
+        }
+        const int64_t o0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D;
+        for (int d = lane; d < D; d += 32) {
+            float O = 0.f;
+            for (int r = 0; r < R; ++r) {
+                const float* mr = merge + ((hw + r * Hc) * G + g) * (D + 2);
+                O += fast_exp2(mr[D] - M) * mr[d];
+            }
+            if (whole)
+                store_out(a.out, o0 + d, O / Lsum, a.out_dtype);
+            else
+                part_o[g * D + d] = O;
+        }
+        if (!whole && lane == 0) {
+            part_ml[g * 2] = M;
+            part_ml[g * 2 + 1] = Lsum;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
-// Policy provides: State, begin(), tile(), publish(), kTensor, kScratch.
+// Policy provides: State, begin(), tile(), write_state(), write_partial(),
+// write_final(), kTensor, kScratch.
 template <class Policy>
 __global__ void __launch_bounds__(32 * 16, 1)
     paged_decode_partial_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                                 const __grid_constant__ CUtensorMap tmv) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_allow_next();
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int G = a.num_q_heads / a.num_kv_heads;
-    const int tile_bytes = a.block_size * a.head_dim * dtype_bytes(a.dtype);
-    const SmemLayout L = smem_layout(a.stages, tile_bytes, a.num_seqs, a.consumer_warps, G,
-                                     a.head_dim, a.block_size, Policy::kScratch);
+    const int Hc = a.heads_per_stage, R = a.warps_per_head, NC = a.consumer_warps;
+    const int chunks = a.num_kv_heads / Hc;
+    const int D = a.head_dim;
+    const int half_bytes = Hc * a.block_size * D * dtype_bytes(a.dtype);
+    const SmemLayout L = smem_layout(a.stages, half_bytes, a.num_seqs, NC, R, G, D, a.block_size,
+                                     Policy::kScratch);
     uint8_t* ring = base + L.ring;
     uint64_t* full = reinterpret_cast<uint64_t*>(base + L.full_bar);
     uint64_t* empty = reinterpret_cast<uint64_t*>(base + L.empty_bar);
@@ -244,38 +339,53 @@ __global__ void __launch_bounds__(32 * 16, 1)
     float* merge = reinterpret_cast<float*>(base + L.merge);
 
     const int tid = threadIdx.x;
+    if (a.stages % R != 0) {  // see decode_plan: the ring must be a multiple of R
+        if (tid == 0 && blockIdx.x == 0) raise_flag(a.status, kFlagBadPlan);
+        return;
+    }
     if (tid == 0) {
         for (int st = 0; st < a.stages; ++st) {
             mbar_init(&full[st], 1);
-            mbar_init(&empty[st], 1);
+            mbar_init(&empty[st], Hc);  // one arrival per head of the chunk
         }
         *abort = 0;
         fence_barrier_init();
-    }
-    if constexpr (Policy::kTensor) {
-        if (tid == 0) {
+        if constexpr (Policy::kTensor) {
             prefetch_tensor_map(&tmk);
             prefetch_tensor_map(&tmv);
         }
     }
-    build_prefix(a, cum, scan);  // ends with __syncthreads
-    if (blockIdx.x == 0) {
-        for (int s = tid; s <= a.num_seqs; s += blockDim.x) a.cum[s] = cum[s];
-    }
+    // Everything above touches only this CTA's shared memory and parameters;
+    // from here on global memory written by the previous launch is read.
+    pdl_wait();
+    build_prefix(a, chunks, cum, scan);  // ends with __syncthreads
     const int64_t W = cum[a.num_seqs];
     const int P = a.num_ctas;
+    if (blockIdx.x == 0 && !a.fused_reduce) {
+        for (int s = tid; s <= a.num_seqs; s += blockDim.x) a.cum[s] = cum[s];
+    }
+    if (a.fused_reduce) {
+        // Sequences with no tokens get zero rows (CTA s mod P writes them).
+        for (int s = blockIdx.x; s < a.num_seqs; s += P) {
+            if (cum[s + 1] != cum[s]) continue;
+            const int64_t o0 = static_cast<int64_t>(s) * a.num_q_heads * D;
+            for (int e = tid; e < a.num_q_heads * D; e += blockDim.x)
+                store_out(a.out, o0 + e, 0.f, a.out_dtype);
+        }
+    }
     const int start = static_cast<int>(static_cast<int64_t>(blockIdx.x) * W / P);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x) + 1) * W / P);
     if (start >= end) return;
 
     const int warp = tid >> 5, lane = tid & 31;
     if (warp == 0) {
-        produce<Policy::kTensor>(a, ring, full, empty, cum, start, end, tile_bytes, &tmk, &tmv,
-                                 abort);
+        produce<Policy::kTensor>(a, ring, full, empty, cum, chunks, start, end, half_bytes, &tmk,
+                                 &tmv, abort);
         return;
     }
     const int w = warp - 1;
-    const int NC = a.consumer_warps;
+    const int hw = w % Hc;  // head within the chunk
+    const int rr = w / Hc;  // replica among the R warps of that head
     float* scratch = Policy::kScratch
                          ? reinterpret_cast<float*>(base + L.scratch) +
                                w * ((a.block_size * G * 4 + 15) & ~15) / 4
@@ -285,60 +395,62 @@ __global__ void __launch_bounds__(32 * 16, 1)
     int seg = start;
     while (seg < end) {
         const int s = find_sequence(cum, a.num_seqs, seg);
-        const int nb = (cum[s + 1] - cum[s]) / a.num_kv_heads;
-        const int h = (seg - cum[s]) / nb;
-        const int pair_a = cum[s] + h * nb;
+        const int nb = (cum[s + 1] - cum[s]) / chunks;
+        const int hc = (seg - cum[s]) / nb;
+        const int pair_a = cum[s] + hc * nb;
         const int pair_b = pair_a + nb;
         const int seg_end = min(pair_b, end);
+        const int h = hc * Hc + hw;
         const int ctx = clamp_context(a, s, false);
         pol.begin(st, a, s, h, G);
-        int first = seg + (((w - (seg - start)) % NC) + NC) % NC;
-        for (int i = first; i < seg_end; i += NC) {
+        const int first = seg + (((rr - (seg - start)) % R) + R) % R;
+        for (int i = first; i < seg_end; i += R) {
             const int t = i - start;
             const int stage = t % a.stages;
             const bool ok = mbar_wait_bounded(&full[stage], (t / a.stages) & 1, abort, a.status);
             if (ok) {
                 const int j = i - pair_a;
                 const int n_valid = min(a.block_size, ctx - j * a.block_size);
-                uint8_t* kt = ring + stage * 2 * tile_bytes;
-                pol.tile(st, a, kt, kt + tile_bytes, n_valid, G, scratch);
+                uint8_t* kt = ring + stage * 2 * half_bytes;
+                pol.tile(st, a, kt, kt + half_bytes, hw, n_valid, G, scratch);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
-        // Merge the consumer warps' states for this segment.
-        float* mw = merge + w * G * (a.head_dim + 2);
-        pol.publish(st, a, mw, G);
-        named_barrier_sync(1, NC * 32);
         const bool whole = (pair_a >= start) && (pair_b <= end);
-        const int pair = s * a.num_kv_heads + h;
-        const int slot = blockIdx.x + pair;
-        const int D = a.head_dim;
-        if (!*abort) {
-            for (int idx = (w << 5) + lane; idx < G * D; idx += NC * 32) {
-                const int g = idx / D, d = idx - g * D;
-                float M = -INFINITY;
-                for (int u = 0; u < NC; ++u) M = fmaxf(M, merge[(u * G + g) * (D + 2) + D]);
-                float Lsum = 0.f, O = 0.f;
-                for (int u = 0; u < NC; ++u) {
-                    const float* mu = merge + (u * G + g) * (D + 2);
-                    const float wgt = fast_exp2(mu[D] - M);
-                    Lsum += wgt * mu[D + 1];
-                    O += wgt * mu[d];
-                }
+        const int pair = s * chunks + hc;
+        const int64_t sl = (static_cast<int64_t>(blockIdx.x + pair) * Hc + hw) * G;
+        bool partial = false;  // this warp wrote the CTA's partial of (s, h)
+        if (R == 1) {
+            if (!*abort) {
                 if (whole) {
-                    const int64_t oi = (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D + d;
-                    store_out(a.out, oi, O / Lsum, a.out_dtype);
+                    pol.write_final(st, a, s, h, G);
                 } else {
-                    a.part_o[(static_cast<int64_t>(slot) * G + g) * D + d] = O;
-                    if (d == 0) {
-                        a.part_ml[(static_cast<int64_t>(slot) * G + g) * 2 + 0] = M;
-                        a.part_ml[(static_cast<int64_t>(slot) * G + g) * 2 + 1] = Lsum;
-                    }
+                    pol.write_partial(st, a, a.part_o + sl * D, a.part_ml + sl * 2, G);
+                    partial = true;
                 }
             }
+        } else {
+            // Merge the R warps of each head through shared memory.
+            pol.write_state(st, a, merge + w * G * (D + 2), D + 2, G);
+            named_barrier_sync(1, NC * 32);
+            if (rr == 0 && !*abort) {
+                combine_replicas(a, merge, hw, Hc, R, G, whole, s, h, a.part_o + sl * D,
+                                 a.part_ml + sl * 2);
+                partial = !whole;
+            }
+            named_barrier_sync(1, NC * 32);
         }
-        named_barrier_sync(1, NC * 32);
+        if (partial && a.fused_reduce) {
+            const int ca = cta_of_item(pair_a, W, P);
+            const int cb = cta_of_item(pair_b - 1, W, P);
+            int nparts = cb - ca + 1;
+            if (W < P) {
+                nparts = 0;
+                for (int c = ca; c <= cb; ++c) nparts += !cta_is_empty(c, W, P);
+            }
+            merge_if_last(a, s, h, hw, pair, nparts, ca, cb, W, G);
+        }
         seg = seg_end;
     }
 }
@@ -358,8 +470,8 @@ cudaError_t launch_partial(const DecodeArgs& a, const CUtensorMap& tmk, const CU
         if (e != cudaSuccess) return e;
         if (cacheable) configured[a.device].store(a.smem_bytes);
     }
-    kern<<<a.num_ctas, 32 * (1 + a.consumer_warps), a.smem_bytes, stream>>>(a, tmk, tmv);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(a.num_ctas), dim3(32 * (1 + a.consumer_warps)),
+                         static_cast<size_t>(a.smem_bytes), stream, a.pdl != 0, a, tmk, tmv);
 }
 
 }  // namespace pkv

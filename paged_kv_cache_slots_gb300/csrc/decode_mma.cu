@@ -106,25 +106,30 @@ struct MmaPolicy {
         st.l[0] = st.l[1] = 0.f;
     }
 
+    // One head's part of a stage: kt/vt point at the stage's K/V, laid out as
+    // [64-element slice][Hc*bs rows][128 B] (128-byte swizzled by the tensor
+    // copy); this warp's head owns rows hw*bs .. hw*bs+bs-1 of every slice.
     __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, uint8_t* kt, uint8_t* vt,
-                                         int n_valid, int, float*) {
+                                         int hw, int n_valid, int, float*) {
         const int lane = threadIdx.x & 31;
         const int bs = a.block_size;
-        const uint32_t half_bytes = static_cast<uint32_t>(bs) * 128u;
-        // Rows past the valid tokens may hold anything (even NaN): zero the V
-        // rows so that 0 * V stays 0 in the PV product.
+        const uint32_t slice_bytes = static_cast<uint32_t>(a.heads_per_stage * bs) * 128u;
+        uint8_t* kh = kt + hw * bs * 128;
+        uint8_t* vh = vt + hw * bs * 128;
+        // Rows past the valid tokens may hold anything (even NaN): zero this
+        // head's V rows there so that 0 * V stays 0 in the PV product.
         if (n_valid < bs) {
-            const int chunks = (bs - n_valid) * (D / 8);  // 16-byte chunks over both halves
-            for (int e = lane; e < chunks; e += 32) {
-                const int hf = e / ((bs - n_valid) * 8);
-                const int r = e - hf * (bs - n_valid) * 8;
-                uint4* p = reinterpret_cast<uint4*>(vt + hf * half_bytes +
-                                                    (n_valid + (r >> 3)) * 128 + ((r & 7) << 4));
+            const int per_slice = (bs - n_valid) * 8;  // 16-byte chunks per slice
+            for (int e = lane; e < per_slice * (D / 64); e += 32) {
+                const int sl = e / per_slice;
+                const int r = e - sl * per_slice;
+                uint4* p = reinterpret_cast<uint4*>(vh + sl * slice_bytes + (n_valid + (r >> 3)) * 128 +
+                                                    ((r & 7) << 4));
                 *p = make_uint4(0u, 0u, 0u, 0u);
             }
             __syncwarp();
         }
-        const uint32_t kb = smem_addr(kt), vb = smem_addr(vt);
+        const uint32_t kb = smem_addr(kh), vb = smem_addr(vh);
         const uint32_t sw = lane & 7;  // 128-byte swizzle key of the rows this lane addresses
         const float sl = a.scale_log2;
         for (int mt = 0; mt < bs / 16; ++mt) {
@@ -136,7 +141,7 @@ struct MmaPolicy {
                 for (int ks = 0; ks < KS; ++ks) {
                     const uint32_t chunk = ((ks & 3) << 1) | (lane >> 4);
                     uint32_t af[4];
-                    ldsm_x4(af, kb + (ks >> 2) * half_bytes + row * 128u + ((chunk ^ sw) << 4));
+                    ldsm_x4(af, kb + (ks >> 2) * slice_bytes + row * 128u + ((chunk ^ sw) << 4));
                     mma16816<DT>(acc, af, st.qb[ks][0], st.qb[ks][1]);
                 }
             }
@@ -161,12 +166,14 @@ struct MmaPolicy {
             const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
             st.l[0] = st.l[0] * al0 + (p0 + p2);
             st.l[1] = st.l[1] * al1 + (p1 + p3);
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-            for (int mi = 0; mi < KS; ++mi) {
-                st.o[mi][0] *= al0;
-                st.o[mi][1] *= al1;
-                st.o[mi][2] *= al0;
-                st.o[mi][3] *= al1;
+                for (int mi = 0; mi < KS; ++mi) {
+                    st.o[mi][0] *= al0;
+                    st.o[mi][1] *= al1;
+                    st.o[mi][2] *= al0;
+                    st.o[mi][3] *= al1;
+                }
             }
             // ---- P^T fragments (k = token, n = head), high + low parts
             uint32_t h01, l01, h23, l23;
@@ -182,7 +189,7 @@ struct MmaPolicy {
                 for (int mi = 0; mi < KS; ++mi) {
                     const uint32_t chunk = ((mi & 3) << 1) | csel;
                     uint32_t af[4];
-                    ldsm_x4_trans(af, vb + (mi >> 2) * half_bytes + row * 128u + ((chunk ^ sw) << 4));
+                    ldsm_x4_trans(af, vb + (mi >> 2) * slice_bytes + row * 128u + ((chunk ^ sw) << 4));
                     mma16816<DT>(st.o[mi], af, bh0, bh1);
                     mma16816<DT>(st.o[mi], af, bl0, bl1);
                 }
@@ -191,36 +198,79 @@ struct MmaPolicy {
         if (n_valid < bs) fence_proxy_async_smem();  // generic writes before the next TMA fill
     }
 
-    __device__ __forceinline__ void publish(const State& st, const DecodeArgs&, float* mw, int G) {
-        const int lane = threadIdx.x & 31;
-        const int g = lane >> 2, c = lane & 3;
-        float l0 = st.l[0], l1 = st.l[1];
+    // Row sums of heads 2c, 2c+1 over the whole warp.
+    __device__ __forceinline__ void row_sums(const State& st, float& l0, float& l1) const {
+        l0 = st.l[0];
+        l1 = st.l[1];
 #pragma unroll
         for (int off = 4; off <= 16; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
+    }
+
+    // O (unnormalised) to o[g*os + d], (max, sum) to ml[g*ms], ml[g*ms + 1].
+    __device__ __forceinline__ void emit(const State& st, float* o, int os, float* ml, int ms,
+                                         int G) const {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        float l0, l1;
+        row_sums(st, l0, l1);
         const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
         for (int mi = 0; mi < KS; ++mi) {
             const int d0 = 16 * mi + g;
             if (h0 < G) {
-                mw[h0 * (D + 2) + d0] = st.o[mi][0];
-                mw[h0 * (D + 2) + d0 + 8] = st.o[mi][2];
+                o[h0 * os + d0] = st.o[mi][0];
+                o[h0 * os + d0 + 8] = st.o[mi][2];
             }
             if (h1 < G) {
-                mw[h1 * (D + 2) + d0] = st.o[mi][1];
-                mw[h1 * (D + 2) + d0 + 8] = st.o[mi][3];
+                o[h1 * os + d0] = st.o[mi][1];
+                o[h1 * os + d0 + 8] = st.o[mi][3];
             }
         }
         if (g == 0) {
             if (h0 < G) {
-                mw[h0 * (D + 2) + D] = st.m[0];
-                mw[h0 * (D + 2) + D + 1] = l0;
+                ml[h0 * ms] = st.m[0];
+                ml[h0 * ms + 1] = l0;
             }
             if (h1 < G) {
-                mw[h1 * (D + 2) + D] = st.m[1];
-                mw[h1 * (D + 2) + D + 1] = l1;
+                ml[h1 * ms] = st.m[1];
+                ml[h1 * ms + 1] = l1;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void write_state(const State& st, const DecodeArgs&, float* dst,
+                                                int stride, int G) const {
+        emit(st, dst, stride, dst + D, stride, G);
+    }
+
+    __device__ __forceinline__ void write_partial(const State& st, const DecodeArgs&, float* o,
+                                                  float* ml, int G) const {
+        emit(st, o, D, ml, 2, G);
+    }
+
+    // out[s][h*G + head][d] = O / l in the output type.
+    __device__ __forceinline__ void write_final(const State& st, const DecodeArgs& a, int s, int h,
+                                                int G) const {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        float l0, l1;
+        row_sums(st, l0, l1);
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
+        const int h0 = 2 * c, h1 = 2 * c + 1;
+        const int64_t base = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+            const int d0 = 16 * mi + g;
+            if (h0 < G) {
+                store_out(a.out, base + h0 * D + d0, st.o[mi][0] * i0, a.out_dtype);
+                store_out(a.out, base + h0 * D + d0 + 8, st.o[mi][2] * i0, a.out_dtype);
+            }
+            if (h1 < G) {
+                store_out(a.out, base + h1 * D + d0, st.o[mi][1] * i1, a.out_dtype);
+                store_out(a.out, base + h1 * D + d0 + 8, st.o[mi][3] * i1, a.out_dtype);
             }
         }
     }

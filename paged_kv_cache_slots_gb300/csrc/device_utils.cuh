@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -17,6 +19,7 @@ constexpr uint32_t kFlagBadBlock = 0x1u;
 constexpr uint32_t kFlagBadSlot = 0x2u;
 constexpr uint32_t kFlagBadContext = 0x4u;
 constexpr uint32_t kFlagTimeout = 0x8u;
+constexpr uint32_t kFlagBadPlan = 0x10u;
 
 // A bounded wait gives up after this many nanoseconds of the global timer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -126,6 +129,20 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Wait until the grid this launch depends on has completed and its memory
+// is visible (a no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next launch in the stream to start being scheduled now; it still
+// waits in pdl_wait() for this grid to complete before touching memory.
+__device__ __forceinline__ void pdl_allow_next() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// L2-coherent load (bypasses L1): for data other CTAs wrote in this launch.
+__device__ __forceinline__ float load_cg(const float* p) { return __ldcg(p); }
+
 // ----------------------------------------------------------- named barrier
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -169,6 +186,24 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int o
         static_cast<__half*>(out)[idx] = __float2half_rn(v);
     else
         static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// Launch `kernel` on `stream`, optionally as a programmatic dependent of the
+// previous launch in the stream (its prologue may overlap that launch's tail).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace pkv

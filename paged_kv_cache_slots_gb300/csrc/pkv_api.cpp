@@ -94,21 +94,26 @@ kv_status_t device_info(int* dev_out, uint32_t** status, int* sms, int* max_smem
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Options {
-    int num_ctas, ctas_per_sm, consumer_warps, kernel, test_stall;
+    int num_ctas, ctas_per_sm, consumer_warps, kernel, heads_per_stage, separate_reduce, no_pdl,
+        test_stall;
 };
 
 kv_status_t read_options(const kv_decode_options_t* o, Options* out) {
-    Options r{0, 1, 8, KV_KERNEL_AUTO, 0};
+    Options r{0, 1, 0, KV_KERNEL_AUTO, 0, 0, 0, 0};
     if (o) {
         if (o->num_ctas < 0 || o->ctas_per_sm < 0 || o->consumer_warps < 0 ||
-            o->consumer_warps > 15 || o->ctas_per_sm > 8)
+            o->consumer_warps > 15 || o->ctas_per_sm > 8 || o->heads_per_stage < 0 ||
+            o->heads_per_stage > 15)
             return fail(KV_ERR_INVALID_ARG, "decode options out of range");
         if (o->kernel != KV_KERNEL_AUTO && o->kernel != KV_KERNEL_FFMA && o->kernel != KV_KERNEL_MMA)
             return fail(KV_ERR_INVALID_ARG, "unknown kernel selector %d", static_cast<int>(o->kernel));
         if (o->num_ctas) r.num_ctas = o->num_ctas;
         if (o->ctas_per_sm) r.ctas_per_sm = o->ctas_per_sm;
-        if (o->consumer_warps) r.consumer_warps = o->consumer_warps;
+        r.consumer_warps = o->consumer_warps;
         r.kernel = o->kernel;
+        r.heads_per_stage = o->heads_per_stage;
+        r.separate_reduce = o->separate_reduce != 0;
+        r.no_pdl = o->no_pdl != 0;
         r.test_stall = o->test_stall != 0;
     }
     *out = r;
@@ -117,10 +122,35 @@ kv_status_t read_options(const kv_decode_options_t* o, Options* out) {
 
 int grid_size(const Options& o, int sms) { return o.num_ctas > 0 ? o.num_ctas : sms * o.ctas_per_sm; }
 
-size_t workspace_bytes_for(int num_seqs, int group, int num_kv_heads, int head_dim, int ctas) {
-    const size_t slots = static_cast<size_t>(ctas) + static_cast<size_t>(num_seqs) * num_kv_heads;
-    return align256(slots * group * head_dim * 4) + align256(slots * group * 2 * 4) +
-           align256(static_cast<size_t>(num_seqs + 1) * 4);
+// Workspace layout: counters [B*Hkv] int32 (must be zero between calls),
+// partial O, partial (max, sum), per-sequence prefix [B+1].  The partial
+// areas are sized for any head chunking: slots * Hc <= (P + B) * Hkv.
+struct WsLayout {
+    size_t counters, part_o, part_ml, cum, total;
+};
+
+WsLayout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int ctas) {
+    WsLayout w;
+    const size_t rows = (static_cast<size_t>(ctas) + num_seqs) * num_q_heads;  // (P + B) * Hkv * G
+    w.counters = 0;
+    w.part_o = align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
+    w.part_ml = w.part_o + align256(rows * head_dim * 4);
+    w.cum = w.part_ml + align256(rows * 2 * 4);
+    w.total = w.cum + align256(static_cast<size_t>(num_seqs + 1) * 4);
+    return w;
+}
+
+// KV heads per pipeline stage: the largest divisor of Hkv whose K slab of one
+// block fits 32 KiB (and, for the tensor copies, 256 box rows).
+int auto_heads_per_stage(int num_kv_heads, int block_size, int head_dim, int dtype, bool tensor) {
+    const int head_bytes = block_size * head_dim * dtype_bytes(dtype);
+    for (int hc = num_kv_heads < 15 ? num_kv_heads : 15; hc > 1; --hc) {
+        if (num_kv_heads % hc) continue;
+        if (hc * head_bytes > 32768) continue;
+        if (tensor && hc * block_size > 256) continue;
+        return hc;
+    }
+    return 1;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -138,14 +168,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D view of one layer's cache: rows = num_blocks*Hkv*bs, row = head_dim
-// elements; box = 64 elements x block_size rows, 128-byte swizzle.
+// elements; box = 64 elements x box_rows rows (Hc heads of one block),
+// 128-byte swizzle.
 kv_status_t encode_cache_map(CUtensorMap* map, const void* base, int dtype, int rows, int head_dim,
-                             int block_size) {
+                             int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(block_size)};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(map, dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                      2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -283,7 +314,8 @@ kv_status_t kv_slot_mapping(const int32_t* block_tables, int max_blocks, const i
         return fail(KV_ERR_UNSUPPORTED, "slots do not fit in int32");
     uint32_t* status = nullptr;
     if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
-    SlotArgs a{block_tables, context_lens, slot_mapping, status, max_blocks, num_seqs, block_size, num_blocks};
+    SlotArgs a{block_tables, context_lens, slot_mapping, status, max_blocks, num_seqs, block_size, num_blocks,
+               1};
     cudaError_t e = launch_slot_mapping(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "slot mapping launch");
     return KV_OK;
@@ -304,7 +336,7 @@ kv_status_t kv_append(kv_pool_t* p, int layer, const int32_t* seq_ids, int n_tok
     uint32_t* status = nullptr;
     if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
     AppendArgs a{seq_ids, k, v, slot_mapping, kc, vc, status, n_tokens, p->cfg.num_kv_heads,
-                 p->cfg.head_dim, p->cfg.block_size, p->cfg.num_blocks, dtype_bytes(p->cfg.dtype)};
+                 p->cfg.head_dim, p->cfg.block_size, p->cfg.num_blocks, dtype_bytes(p->cfg.dtype), 1};
     cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return KV_OK;
@@ -324,8 +356,18 @@ kv_status_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_
         if (!g.ok) return fail(KV_ERR_CUDA, "cannot select device %d", device);
         if (kv_status_t st = device_info(nullptr, nullptr, &sms, nullptr, nullptr)) return st;
     }
-    *bytes = workspace_bytes_for(num_seqs, num_q_heads / num_kv_heads, num_kv_heads, head_dim,
-                                 grid_size(o, sms));
+    *bytes = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, grid_size(o, sms)).total;
+    return KV_OK;
+}
+
+kv_status_t paged_decode_workspace_init(void* workspace, size_t workspace_bytes, int num_seqs,
+                                        int num_kv_heads, void* stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0) return fail(KV_ERR_INVALID_ARG, "workspace init: sizes");
+    const size_t n = static_cast<size_t>(num_seqs) * num_kv_heads * 4;
+    if (n == 0) return KV_OK;
+    if (!workspace || workspace_bytes < n) return fail(KV_ERR_INVALID_ARG, "workspace init: buffer");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     return KV_OK;
 }
 
@@ -371,20 +413,42 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
     uint32_t* status = nullptr;
     if (kv_status_t st = device_info(&dev, &status, &sms, &max_smem, &smem_sm)) return st;
     const int P = grid_size(o, sms);
-    const size_t need = workspace_bytes_for(num_seqs, G, num_kv_heads, head_dim, P);
-    if (workspace_bytes < need)
-        return fail(KV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    const WsLayout wl = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, P);
+    if (workspace_bytes < wl.total)
+        return fail(KV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes,
+                    wl.total);
+    // Head chunking and warps: Hc KV heads per stage, R warps per head.
+    int hc = o.heads_per_stage;
+    if (hc == 0) {
+        hc = auto_heads_per_stage(num_kv_heads, block_size, head_dim, dtype, kernel == KV_KERNEL_MMA);
+    } else if (num_kv_heads % hc) {
+        return fail(KV_ERR_INVALID_ARG, "heads_per_stage %d does not divide num_kv_heads %d", hc,
+                    num_kv_heads);
+    }
+    if (kernel == KV_KERNEL_MMA && hc * block_size > 256)
+        return fail(KV_ERR_UNSUPPORTED, "heads_per_stage * block_size must be <= 256 for the tensor copies");
+    const int target = o.consumer_warps ? o.consumer_warps : 8;
+    int R = target / hc;
+    if (R < 1) R = 1;
+    while (hc * R > 15 && R > 1) --R;
+    if (hc * R > 15) return fail(KV_ERR_UNSUPPORTED, "more than 15 consumer warps");
     int budget = max_smem;
     if (o.ctas_per_sm > 1) {
         const int share = smem_sm / o.ctas_per_sm - 1024;
         if (share < budget) budget = share;
     }
+    // Fewer warps per head when the ring would hold less than two stages per
+    // replica (each replica owns every R-th stage).
     DecodePlan plan{};
-    if (!decode_plan(kernel, dtype, head_dim, block_size, G, num_seqs, o.consumer_warps, budget, &plan))
-        return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages for these sizes");
+    bool planned = false;
+    for (; R >= 1; --R) {
+        planned = decode_plan(kernel, dtype, head_dim, block_size, G, num_seqs, hc, R, budget, &plan);
+        if (planned && (plan.stages >= 2 * R || R == 1)) break;
+        if (planned && o.consumer_warps) break;  // an explicit warp count is kept if it fits at all
+    }
+    if (!planned) return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages for these sizes");
 
     char* ws = static_cast<char*>(workspace);
-    const size_t slots = static_cast<size_t>(P) + static_cast<size_t>(num_seqs) * num_kv_heads;
     DecodeArgs a{};
     a.q = q;
     a.k_cache = k_cache;
@@ -392,9 +456,10 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.out = out;
-    a.part_o = reinterpret_cast<float*>(ws);
-    a.part_ml = reinterpret_cast<float*>(ws + align256(slots * G * head_dim * 4));
-    a.cum = reinterpret_cast<int32_t*>(ws + align256(slots * G * head_dim * 4) + align256(slots * G * 2 * 4));
+    a.counters = reinterpret_cast<int32_t*>(ws + wl.counters);
+    a.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+    a.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
+    a.cum = reinterpret_cast<int32_t*>(ws + wl.cum);
     a.status = status;
     a.num_blocks = num_blocks;
     a.max_blocks = max_blocks;
@@ -407,9 +472,13 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
     a.out_dtype = out_dtype;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.num_ctas = P;
-    a.consumer_warps = o.consumer_warps;
+    a.heads_per_stage = hc;
+    a.warps_per_head = R;
+    a.consumer_warps = hc * R;
     a.stages = plan.stages;
     a.smem_bytes = plan.smem_bytes;
+    a.fused_reduce = o.separate_reduce ? 0 : 1;
+    a.pdl = o.no_pdl ? 0 : 1;
     a.test_stall = o.test_stall;
     a.device = dev;
 
@@ -418,15 +487,17 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
     if (kernel == KV_KERNEL_MMA) {
         CUtensorMap tk, tv;
         const int rows = num_blocks * num_kv_heads * block_size;
-        if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, block_size)) return st;
-        if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, block_size)) return st;
+        if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, hc * block_size)) return st;
+        if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, hc * block_size)) return st;
         e = launch_decode_mma(a, tk, tv, s);
     } else {
         e = launch_decode_ffma(a, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode partial launch");
-    e = launch_decode_reduce(a, s);
-    if (e != cudaSuccess) return cuda_fail(e, "decode reduce launch");
+    if (!a.fused_reduce) {
+        e = launch_decode_reduce(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode reduce launch");
+    }
     return KV_OK;
 }
 

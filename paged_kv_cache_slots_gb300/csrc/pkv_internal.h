@@ -23,6 +23,7 @@ struct AppendArgs {
     void* v_cache;
     uint32_t* status;             // device status word
     int n_tokens, num_kv_heads, head_dim, block_size, num_blocks, elem_bytes;
+    int pdl;
 };
 
 struct SlotArgs {
@@ -31,11 +32,16 @@ struct SlotArgs {
     int32_t* slot_mapping;
     uint32_t* status;
     int max_blocks, num_seqs, block_size, num_blocks;
+    int pdl;
 };
 
-// Everything the split-context decode kernels need.  The flattened work space
-// is the (sequence, kv head, logical block) triples in that order; CTA c of
-// num_ctas owns [c*W/P, (c+1)*W/P) of it.
+// Everything the split-context decode kernels need.
+//
+// Work items are (sequence, head chunk, logical block) triples in that order;
+// a head chunk is `heads_per_stage` consecutive KV heads, whose K (and V)
+// rows of one block are contiguous in the pool, so one item is one pipeline
+// stage of two contiguous copies.  W = chunks * sum_s ceil(ctx_s / bs);
+// CTA c of num_ctas owns items [c*W/P, (c+1)*W/P).
 struct DecodeArgs {
     const void* q;
     const void* k_cache;
@@ -43,28 +49,35 @@ struct DecodeArgs {
     const int32_t* block_tables;
     const int32_t* context_lens;
     void* out;
-    float* part_o;    // [slots][G][D]    unnormalised partial outputs
-    float* part_ml;   // [slots][G][2]    running max (log2 units) and sum
-    int32_t* cum;     // [num_seqs + 1]   exclusive prefix of tiles per sequence
+    float* part_o;      // [slots][Hc][G][D]  unnormalised partial outputs
+    float* part_ml;     // [slots][Hc][G][2]  running max (log2 units) and sum
+    int32_t* cum;       // [num_seqs + 1]     exclusive prefix of items per sequence
+    int32_t* counters;  // [num_seqs * Hkv]   partials merged so far (zero between calls)
     uint32_t* status;
     int num_blocks, max_blocks, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     int dtype, out_dtype;
-    float scale_log2;  // scale * log2(e): scores are kept in base-2 units
-    int num_ctas, consumer_warps, stages;
+    float scale_log2;     // scale * log2(e): scores are kept in base-2 units
+    int num_ctas;         // persistent grid size P
+    int heads_per_stage;  // Hc: KV heads per pipeline stage (divides Hkv)
+    int warps_per_head;   // R: consumer warps sharing one head's items
+    int consumer_warps;   // Hc * R
+    int stages;
     int smem_bytes;
-    int test_stall;  // testing only: see kv_decode_options_t
-    int device;      // CUDA ordinal the launch targets
+    int fused_reduce;     // 1: the last CTA of a split pair merges it (no reduce kernel)
+    int pdl;              // 1: launch with programmatic dependent launch
+    int test_stall;       // testing only: see kv_decode_options_t
+    int device;           // CUDA ordinal the launch targets
 };
 
 // Shared-memory plan of the partial kernel.
 struct DecodePlan {
     int stages;
     int smem_bytes;
-    int tile_bytes;  // one (block, kv head) tile of K (same for V)
+    int stage_half_bytes;  // K (or V) bytes of one stage: Hc * bs * D * elem
 };
 
 bool decode_plan(int kernel, int dtype, int head_dim, int block_size, int group, int num_seqs,
-                 int consumer_warps, int smem_budget, DecodePlan* plan);
+                 int heads_per_stage, int warps_per_head, int smem_budget, DecodePlan* plan);
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_slot_mapping(const SlotArgs& a, cudaStream_t stream);

@@ -51,6 +51,7 @@ def attend(q, kc, vc, tables, ctx, scale, out_dtype=None, **opts):
     n = pkv.workspace_bytes(B, Hq, kc.shape[1], D, q.device,
                             **{k: v for k, v in opts.items() if k != "test_stall"})
     ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=q.device)
+    pkv.workspace_init(ws, B, kc.shape[1])  # only the merge counters must start at zero
     return pkv.paged_decode_attention(q, kc, vc, tables, ctx, scale, out=out, out_dtype=out_dtype,
                                       workspace=ws, **opts)
 

@@ -120,11 +120,18 @@ def test_block_size_8_uses_the_ffma_kernel():
     _full_small_check(spec, kernels=("auto", "ffma"))
 
 
+SPLITS = [dict(), dict(num_ctas=1, consumer_warps=8), dict(num_ctas=2, consumer_warps=1),
+          dict(num_ctas=7, consumer_warps=3), dict(num_ctas=64), dict(num_ctas=1000, consumer_warps=15),
+          dict(num_ctas=152, consumer_warps=4), dict(heads_per_stage=1), dict(heads_per_stage=2),
+          dict(heads_per_stage=4, consumer_warps=12), dict(separate_reduce=True),
+          dict(separate_reduce=True, num_ctas=1000), dict(pdl=False), dict(ctas_per_sm=2)]
+
+
 @pytest.mark.parametrize("kernel", ["mma", "ffma"])
 def test_split_and_warp_counts_agree(kernel):
-    """Any persistent-grid size or consumer-warp count gives the same result."""
+    """Any grid size, head chunking, warp count or reduce mode gives the same result."""
     spec = small_spec("splits", num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16,
-                      dtype="f16", seed=5, ctx=(700, 1, 333, 2048, 16, 45))
+                      dtype="f16", seed=5, ctx=(700, 1, 333, 2048, 16, 45, 0))
     pl = make_placement(spec)
     case = SmallCase(spec, pl)
     _, _, _, ref = case.oracle()
@@ -132,15 +139,33 @@ def test_split_and_warp_counts_agree(kernel):
     slots = pkv.slot_mapping(d["tables"], d["ctx"], spec.block_size, pl.num_blocks)
     d["pool"].append(0, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
     outs = []
-    for num_ctas, warps in [(0, 0), (1, 8), (2, 1), (7, 3), (64, 8), (1000, 15), (152, 4)]:
-        out = attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"],
-                                         spec.attn_scale, out_dtype=torch.float32, kernel=kernel,
-                                         num_ctas=num_ctas, consumer_warps=warps)
-        check_output(out, ref, f"num_ctas={num_ctas} warps={warps}")
+    for opts in SPLITS:
+        out = attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                     out_dtype=torch.float32, kernel=kernel, **opts)
+        check_output(out, ref, f"{opts}")
         outs.append(out)
-    for o in outs[1:]:
-        assert torch.max(torch.abs(o - outs[0])).item() <= 2e-5
+    for o, opts in zip(outs[1:], SPLITS[1:]):
+        assert torch.max(torch.abs(o - outs[0])).item() <= 2e-5, opts
     assert pkv.device_status() == (0, 0)
+
+
+def test_workspace_is_reusable_across_calls():
+    """The merge counters return to zero: the same workspace serves many calls."""
+    spec = small_spec("reuse", num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                      dtype="bf16", seed=6, ctx=(900, 37, 2000))
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    _, _, _, ref = case.oracle()
+    d = case.device()
+    slots = pkv.slot_mapping(d["tables"], d["ctx"], spec.block_size, pl.num_blocks)
+    d["pool"].append(0, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
+    ws = pkv.make_workspace(3, 8, 2, 128, num_ctas=40)
+    for _ in range(5):
+        out = torch.full((3, 8, 128), float("nan"), device="cuda")
+        pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                                   out=out, out_dtype=torch.float32, workspace=ws, num_ctas=40)
+        check_output(out, ref, "reused workspace")
+    assert int(ws[:3 * 2 * 4].view(torch.int32).abs().sum().item()) == 0
 
 
 @pytest.mark.parametrize("kernel", ["mma", "ffma"])
@@ -248,6 +273,7 @@ def test_cuda_graph_capture_of_a_step():
     _, _, _, ref = case.oracle()
     d = case.device()
     ws = torch.full((pkv.workspace_bytes(8, 32, 8, 128),), 0xFF, dtype=torch.uint8, device="cuda")
+    pkv.workspace_init(ws, 8, 8)
     out = torch.full((8, 32, 128), float("nan"), dtype=torch.float32, device="cuda")
     slots = torch.empty(8, dtype=torch.int32, device="cuda")
     # Warm-up outside the capture (loads the kernels, sets their attributes).
