@@ -57,6 +57,8 @@ def parse_args():
     p.add_argument("--heads-per-stage", type=int, default=0, help="0: library default")
     p.add_argument("--separate-reduce", action="store_true")
     p.add_argument("--no-pdl", action="store_true")
+    p.add_argument("--unfused", action="store_true",
+                   help="slot mapping + append + attention as separate calls instead of one fused call per layer")
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: run the first N layers (the JSON line then names N)")
     p.add_argument("--e2e-steps", type=int, default=30)
@@ -189,10 +191,10 @@ class ClockSampler:
 class Step:
     """Device state of the benchmark workload and one decode step through the library."""
 
-    def __init__(self, spec, kernel, device, **opts):
+    def __init__(self, spec, kernel, device, fused=True, **opts):
         import paged_kv_cache_slots_gb300 as pkv
         self.pkv = pkv
-        self.spec, self.kernel, self.dev = spec, kernel, device
+        self.spec, self.kernel, self.dev, self.fused = spec, kernel, device, fused
         self.opts = dict(kernel=kernel, **opts)
         self.pl = make_placement(spec)
         s, pl = spec, self.pl
@@ -217,17 +219,25 @@ class Step:
         self.slots = torch.empty(B, dtype=torch.int32, device=device)
         self.out = torch.empty((s.num_layers, B, s.num_q_heads, s.head_dim), dtype=s.torch_dtype, device=device)
         self.ws = pkv.make_workspace(B, s.num_q_heads, s.num_kv_heads, s.head_dim, device, **self.opts)
-        self.launches_per_step = 1 + (3 if self.opts.get("separate_reduce") else 2) * s.num_layers
+        per_layer = (2 if self.opts.get("separate_reduce") else 1) + (0 if fused else 1)
+        self.launches_per_step = (0 if fused else 1) + per_layer * s.num_layers
 
     def run(self, events=None):
         s, pkv = self.spec, self.pkv
-        pkv.slot_mapping(self.tables, self.ctx, s.block_size, self.pl.num_blocks, out=self.slots)
+        if not self.fused:
+            pkv.slot_mapping(self.tables, self.ctx, s.block_size, self.pl.num_blocks, out=self.slots)
         for l, (kc, vc) in enumerate(self.layers):
-            self.pool.append(l, self.kn[l], self.vn[l], self.slots, seq_ids=self.seq_ids)
             if events is not None:
                 events[l][0].record()
-            pkv.paged_decode_attention(self.q[l], kc, vc, self.tables, self.ctx, s.attn_scale,
-                                       out=self.out[l], workspace=self.ws, **self.opts)
+            if self.fused:
+                pkv.paged_decode_append_attention(self.q[l], self.kn[l], self.vn[l], kc, vc, self.tables,
+                                                  self.ctx, s.attn_scale, seq_ids=self.seq_ids,
+                                                  out=self.out[l], slot_mapping=self.slots,
+                                                  workspace=self.ws, **self.opts)
+            else:
+                self.pool.append(l, self.kn[l], self.vn[l], self.slots, seq_ids=self.seq_ids)
+                pkv.paged_decode_attention(self.q[l], kc, vc, self.tables, self.ctx, s.attn_scale,
+                                           out=self.out[l], workspace=self.ws, **self.opts)
             if events is not None:
                 events[l][1].record()
 
@@ -242,7 +252,8 @@ def bench_ours(args, world, rank, local):
     spec = SPECS[args.workload]
     if args.layers:
         spec = dataclasses.replace(spec, num_layers=args.layers)
-    step = Step(spec, args.kernel, dev, consumer_warps=args.consumer_warps, ctas_per_sm=args.ctas_per_sm,
+    step = Step(spec, args.kernel, dev, fused=not args.unfused, consumer_warps=args.consumer_warps,
+                ctas_per_sm=args.ctas_per_sm,
                 heads_per_stage=args.heads_per_stage, separate_reduce=args.separate_reduce,
                 pdl=not args.no_pdl)
     pl = step.pl
@@ -303,9 +314,12 @@ def bench_ours(args, world, rank, local):
     torch.cuda.synchronize()
     launch_ms = statistics.mean(a.elapsed_time(b) for e in evs for a, b in e)
     peak, peak_kind = measured_peaks()
-    achieved = bytes_layer.attention / (launch_ms * 1e-3) / 1e9
+    launch_bytes = bytes_layer.attention + (bytes_layer.append if step.fused else 0)
+    achieved = launch_bytes / (launch_ms * 1e-3) / 1e9
     kernel_name = "paged_decode_partial_kernel<MmaPolicy>" if step.kernel != "ffma" else \
         "paged_decode_partial_kernel<FfmaPolicy>"
+    if step.fused:
+        kernel_name += " with fused append"
     traffic = recorded_traffic(kernel_name, spec.name)
 
     # End to end through the public API with host buffers (pinned), copies timed.
@@ -369,7 +383,7 @@ def bench_ours(args, world, rank, local):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kernel_name + (" + paged_decode_reduce_kernel" if args.separate_reduce
                                               else " (cross-CTA merge fused)"),
-                     "algorithmic_bytes_per_launch": bytes_layer.attention,
+                     "algorithmic_bytes_per_launch": launch_bytes,
                      "launch_ms": round(launch_ms, 5), "peak_source": f"{peak_kind} hbm_gbs"},
         "clocks": clock,
     }

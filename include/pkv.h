@@ -229,6 +229,32 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
                                    kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
                                    const kv_decode_options_t* opts, void* stream);
 
+/* One layer of one decode step in a single kernel: the append of every
+ * sequence's newest token followed by the attention that reads it.
+ * Equivalent to kv_slot_mapping + kv_append + paged_decode_attention with the
+ * same arguments ("vLLM Architecture and Installation", Example 3: write the
+ * new rows through the slot mapping, then read the history through the block
+ * table), without the two extra launches.  For each sequence s with
+ * context_lens[s] >= 1 (and seq_ids == NULL or seq_ids[s] >= 0) the rows
+ * k_new[s], v_new[s] ([num_seqs][num_kv_heads][head_dim], device, 16-byte
+ * aligned) are written to position context_lens[s] - 1, i.e. slot
+ * table[s][p / bs] * bs + p % bs, and that position takes part in this
+ * step's attention.  The block holding that slot must not be shared with
+ * another sequence of the batch (copy-on-write is the caller's job).
+ * slot_mapping: device int32[num_seqs] that receives the slots (-1 for an
+ * empty sequence), or NULL.  The other arguments are those of
+ * paged_decode_attention; k_cache and v_cache are written. */
+kv_status_t paged_decode_append_attention(const void* q, const void* k_new, const void* v_new,
+                                          const int32_t* seq_ids, void* k_cache, void* v_cache,
+                                          int num_blocks, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, kv_dtype_t dtype,
+                                          float scale, void* out, kv_dtype_t out_dtype,
+                                          int32_t* slot_mapping, void* workspace,
+                                          size_t workspace_bytes, const kv_decode_options_t* opts,
+                                          void* stream);
+
 /* Synchronise `stream`, then read and clear the status word of `device`.
  * flags_out (may be NULL) receives the KV_FLAG_* bits.  Returns KV_OK when no
  * bit was set, KV_ERR_DEVICE_TIMEOUT if the timeout bit was set, else

@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "KVError", "KVPool", "BlockAllocator", "kv_pool_bytes", "slot_mapping", "workspace_bytes",
     "paged_decode_attention", "device_status", "library_path", "load_library", "workspace_init",
-    "make_workspace",
+    "make_workspace", "paged_decode_append_attention",
 ]
 
 KV_F32, KV_F16, KV_BF16 = 0, 1, 2
@@ -76,6 +76,9 @@ def _declare(lib):
         "paged_decode_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P,
                                        I, P, SZ, ctypes.POINTER(_DecodeOptions), P]),
         "paged_decode_workspace_init": (I, [P, SZ, I, I, P]),
+        "paged_decode_append_attention": (I, [P, P, P, P, P, P, I, P, I, P, I, I, I, I, I, I,
+                                              ctypes.c_float, P, I, P, P, SZ,
+                                              ctypes.POINTER(_DecodeOptions), P]),
         "kv_device_status": (I, [I, P, U32P]),
         "kv_allocator_create": (I, [I, I, I, ctypes.POINTER(P)]),
         "kv_allocator_destroy": (None, [P]),
@@ -279,6 +282,43 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         _ptr(context_lens), B, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale), _ptr(out),
         DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(), ctypes.byref(o),
         _stream(q, stream)), lib)
+    return out
+
+
+def paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                                  scale: float, seq_ids=None, out=None, out_dtype=None,
+                                  slot_mapping=None, workspace=None, stream=None, **opts):
+    """One layer of a decode step in one kernel: append k_new/v_new ([B, Hkv, D]) at
+    position context_lens - 1 of every sequence, then attend (see paged_decode_attention).
+
+    seq_ids: optional int32 [B]; a negative entry skips the append of that sequence.
+    slot_mapping: optional int32 [B] output receiving the newest-token slots.
+    """
+    lib = load_library()
+    B, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    _need(D == D2 and tuple(v_cache.shape) == tuple(k_cache.shape), "cache shapes")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype == k_new.dtype == v_new.dtype, "one dtype")
+    _need(tuple(k_new.shape) == (B, Hkv, D) and k_new.shape == v_new.shape, "k_new/v_new [B, Hkv, D]")
+    _need(all(t.is_contiguous() for t in (q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)),
+          "contiguous inputs")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32, "int32 tables")
+    _need(block_tables.shape[0] == B and context_lens.shape[0] == B, "one table row and length per sequence")
+    _need(seq_ids is None or (seq_ids.dtype == torch.int32 and seq_ids.shape[0] == B), "seq_ids int32 [B]")
+    _need(slot_mapping is None or (slot_mapping.dtype == torch.int32 and slot_mapping.shape[0] == B),
+          "slot_mapping int32 [B]")
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    _need(out.dtype == out_dtype and tuple(out.shape) == (B, Hq, D) and out.is_contiguous(), "out")
+    o = _options(**opts)
+    if workspace is None:
+        workspace = make_workspace(B, Hq, Hkv, D, q.device, **opts)
+    _check(lib.paged_decode_append_attention(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_ids), _ptr(k_cache), _ptr(v_cache), NB,
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
+        DTYPE_CODE[q.dtype], float(scale), _ptr(out), DTYPE_CODE[out_dtype], _ptr(slot_mapping),
+        _ptr(workspace), workspace.numel(), ctypes.byref(o), _stream(q, stream)), lib)
     return out
 
 

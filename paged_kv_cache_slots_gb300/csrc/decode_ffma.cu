@@ -73,6 +73,7 @@ struct FfmaPolicy {
     static constexpr bool kTensor = false;
     static constexpr bool kScratch = true;
     static constexpr int VD = D / 32;
+    static constexpr int kD = D;
     using T = typename Elem<DT>::T;
 
     struct State {
@@ -167,6 +168,12 @@ struct FfmaPolicy {
             }
         }
         __syncwarp();
+    }
+
+    // 16-byte chunk q of row r of head hw's tile (plain [Hc][bs][D] layout).
+    __device__ __forceinline__ void patch_chunk(const DecodeArgs& a, uint8_t* t, int hw, int r, int q,
+                                                uint4 val) const {
+        *(reinterpret_cast<uint4*>(t + (static_cast<int64_t>(hw) * a.block_size + r) * D * sizeof(T)) + q) = val;
     }
 
     // O (unnormalised) to o[g*os + d], (max, sum) to ml[g*ms], ml[g*ms + 1].

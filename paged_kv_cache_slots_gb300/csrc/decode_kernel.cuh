@@ -236,11 +236,104 @@ static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* ful
 // ------------------------------------------------- merge of split pairs
 // Called by one warp per (sequence s, KV head h) after it wrote its partial
 // for slot c + pair.  Counts the arrival; the warp that arrives last merges
-// the nparts partials of (s, h) into the output and resets the counter.
-static __device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, int pair, int nparts,
-                              int ca, int cb, int64_t W, int G) {
+// the partials of (s, h) into the output and resets the counter.
+//
+// The merge keeps its L2 round trips few: lane l fetches (max, sum) of part
+// l / G, head l % G in one load, the weights are shared by shuffles, and the
+// partial outputs of two parts (all G heads, D/32 dims per lane) are loaded
+// together before they are used.
+template <int G, int D>
+__device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, int hw, int pair,
+                                            int ca, int cb, int64_t W) {
+    constexpr int VD = D / 32;
+    constexpr int kParts = 32 / G;  // parts handled per round
     const int lane = threadIdx.x & 31;
-    const int D = a.head_dim, Hc = a.heads_per_stage;
+    const int Hc = a.heads_per_stage;
+    const int64_t P = a.num_ctas;
+    const int kp = lane / G, kg = lane % G;  // this lane's (part, head) for the (max, sum) loads
+    float acc[G][VD];
+    float M[G], Lsum[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        M[g] = -INFINITY;
+        Lsum[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < VD; ++i) acc[g][i] = 0.f;
+    }
+    int c = ca;
+    while (c <= cb) {
+        // This lane's part: the kp-th CTA with a non-empty item range from c on.
+        int my_c = c;
+        while (my_c <= cb && cta_is_empty(my_c, W, P)) ++my_c;
+        for (int j = 0; j < kp && my_c <= cb; ++j) {
+            ++my_c;
+            while (my_c <= cb && cta_is_empty(my_c, W, P)) ++my_c;
+        }
+        if (my_c > cb) my_c = -1;
+        const int n = __popc(__ballot_sync(0xffffffffu, my_c >= 0 && kg == 0));
+        if (n == 0) break;
+        c = __shfl_sync(0xffffffffu, my_c, (n - 1) * G) + 1;
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (my_c >= 0) {
+            const int64_t sl = ((static_cast<int64_t>(my_c) + pair) * Hc + hw) * G + kg;
+            ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + sl * 2));
+        }
+        // New running max per head; rescale what was accumulated so far.
+        float w_lane = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float mg = -INFINITY;
+            for (int k = 0; k < n; ++k) mg = fmaxf(mg, __shfl_sync(0xffffffffu, ml.x, k * G + g));
+            const float mn = fmaxf(M[g], mg);
+            const float al = fast_exp2(M[g] - mn);
+            M[g] = mn;
+            Lsum[g] *= al;
+#pragma unroll
+            for (int i = 0; i < VD; ++i) acc[g][i] *= al;
+            if (kg == g && my_c >= 0) w_lane = fast_exp2(ml.x - mn);
+        }
+        const float wl = w_lane * ml.y;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            for (int k = 0; k < n; ++k) Lsum[g] += __shfl_sync(0xffffffffu, wl, k * G + g);
+        // Partial outputs, two parts per round of loads.
+        for (int k = 0; k < n; k += 2) {
+            const int c0 = __shfl_sync(0xffffffffu, my_c, k * G);
+            const int c1 = __shfl_sync(0xffffffffu, my_c, (k + 1 < n ? k + 1 : k) * G);
+            const int64_t s0 = ((static_cast<int64_t>(c0) + pair) * Hc + hw) * G;
+            const int64_t s1 = ((static_cast<int64_t>(c1) + pair) * Hc + hw) * G;
+            float v0[G][VD], v1[G][VD];
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int i = 0; i < VD; ++i) {
+                    v0[g][i] = __ldcg(a.part_o + (s0 + g) * D + lane + 32 * i);
+                    v1[g][i] = __ldcg(a.part_o + (s1 + g) * D + lane + 32 * i);
+                }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float w0 = __shfl_sync(0xffffffffu, w_lane, k * G + g);
+                float w1 = __shfl_sync(0xffffffffu, w_lane, (k + 1 < n ? k + 1 : k) * G + g);
+                if (k + 1 >= n) w1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < VD; ++i) acc[g][i] += w0 * v0[g][i] + w1 * v1[g][i];
+            }
+        }
+    }
+    const int64_t o0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float inv = 1.f / Lsum[g];
+#pragma unroll
+        for (int i = 0; i < VD; ++i)
+            store_out(a.out, o0 + g * D + lane + 32 * i, acc[g][i] * inv, a.out_dtype);
+    }
+}
+
+template <int G, int D>
+__device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, int pair, int nparts,
+                              int ca, int cb, int64_t W) {
+    const int lane = threadIdx.x & 31;
     int32_t* counter = a.counters + static_cast<int64_t>(s) * a.num_kv_heads + h;
     __threadfence();
     __syncwarp();
@@ -249,32 +342,7 @@ static __device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, 
     prev = __shfl_sync(0xffffffffu, prev, 0);
     if (prev != nparts - 1) return;
     __threadfence();
-    const int64_t P = a.num_ctas;
-    for (int g = 0; g < G; ++g) {
-        float M = -INFINITY;
-        for (int c = ca; c <= cb; ++c) {
-            if (cta_is_empty(c, W, P)) continue;
-            const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g;
-            M = fmaxf(M, load_cg(a.part_ml + sl * 2));
-        }
-        float Lsum = 0.f;
-        for (int c = ca; c <= cb; ++c) {
-            if (cta_is_empty(c, W, P)) continue;
-            const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g;
-            Lsum += fast_exp2(load_cg(a.part_ml + sl * 2) - M) * load_cg(a.part_ml + sl * 2 + 1);
-        }
-        const float inv = 1.f / Lsum;
-        const int64_t o0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D;
-        for (int d = lane; d < D; d += 32) {
-            float O = 0.f;
-            for (int c = ca; c <= cb; ++c) {
-                if (cta_is_empty(c, W, P)) continue;
-                const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g;
-                O += fast_exp2(load_cg(a.part_ml + sl * 2) - M) * load_cg(a.part_o + sl * D + d);
-            }
-            store_out(a.out, o0 + d, O * inv, a.out_dtype);
-        }
-    }
+    merge_parts<G, D>(a, s, h, hw, pair, ca, cb, W);
     __syncwarp();
     if (lane == 0) *counter = 0;
 }
@@ -310,6 +378,38 @@ static __device__ void combine_replicas(const DecodeArgs& a, const float* merge,
             part_ml[g * 2 + 1] = Lsum;
         }
     }
+}
+
+// ------------------------------------------------------------ fused append
+// The warp that consumes the last block of (s, h) writes the new token's K
+// and V rows (k_new[s][h], v_new[s][h]) into row r of that block: into the
+// staged tile in shared memory (so this step attends to it) and into the
+// pool in HBM (so later steps do).  Returns whether it wrote.
+template <class Policy>
+__device__ __forceinline__ bool append_row(const DecodeArgs& a, const Policy& pol, uint8_t* kt,
+                                           uint8_t* vt, int s, int h, int hw, int j, int r) {
+    const int lane = threadIdx.x & 31;
+    const int blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + j];
+    if (blk < 0 || blk >= a.num_blocks) return false;  // already flagged by the producer
+    // The slot is reported whether or not this sequence appends (as kv_slot_mapping does).
+    if (a.slot_out && h == 0 && lane == 0) a.slot_out[s] = blk * a.block_size + r;
+    if (a.append_ids && a.append_ids[s] < 0) return false;
+    const int eb = dtype_bytes(a.dtype);
+    const int nchunk = a.head_dim * eb / 16;  // 16-byte chunks of one row
+    const int64_t src = (static_cast<int64_t>(s) * a.num_kv_heads + h) * a.head_dim * eb;
+    const int64_t dst = ((static_cast<int64_t>(blk) * a.num_kv_heads + h) * a.block_size + r) *
+                        static_cast<int64_t>(a.head_dim) * eb;
+    for (int e = lane; e < 2 * nchunk; e += 32) {
+        const bool isv = e >= nchunk;
+        const int q = isv ? e - nchunk : e;
+        const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                              static_cast<const char*>(isv ? a.v_new : a.k_new) + src) + q);
+        *(reinterpret_cast<uint4*>(const_cast<char*>(
+              static_cast<const char*>(isv ? a.v_cache : a.k_cache)) + dst) + q) = val;
+        pol.patch_chunk(a, isv ? vt : kt, hw, r, q, val);
+    }
+    __syncwarp();
+    return true;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -364,14 +464,14 @@ __global__ void __launch_bounds__(32 * 16, 1)
     if (blockIdx.x == 0 && !a.fused_reduce) {
         for (int s = tid; s <= a.num_seqs; s += blockDim.x) a.cum[s] = cum[s];
     }
-    if (a.fused_reduce) {
-        // Sequences with no tokens get zero rows (CTA s mod P writes them).
-        for (int s = blockIdx.x; s < a.num_seqs; s += P) {
-            if (cum[s + 1] != cum[s]) continue;
-            const int64_t o0 = static_cast<int64_t>(s) * a.num_q_heads * D;
-            for (int e = tid; e < a.num_q_heads * D; e += blockDim.x)
-                store_out(a.out, o0 + e, 0.f, a.out_dtype);
-        }
+    // Sequences with no tokens: zero rows (fused merge) and slot -1 (CTA s mod P).
+    for (int s = blockIdx.x; s < a.num_seqs; s += P) {
+        if (cum[s + 1] != cum[s]) continue;
+        if (a.slot_out && tid == 0) a.slot_out[s] = -1;
+        if (!a.fused_reduce) continue;
+        const int64_t o0 = static_cast<int64_t>(s) * a.num_q_heads * D;
+        for (int e = tid; e < a.num_q_heads * D; e += blockDim.x)
+            store_out(a.out, o0 + e, 0.f, a.out_dtype);
     }
     const int start = static_cast<int>(static_cast<int64_t>(blockIdx.x) * W / P);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x) + 1) * W / P);
@@ -412,7 +512,9 @@ __global__ void __launch_bounds__(32 * 16, 1)
                 const int j = i - pair_a;
                 const int n_valid = min(a.block_size, ctx - j * a.block_size);
                 uint8_t* kt = ring + stage * 2 * half_bytes;
+                const bool patched = a.k_new && j == nb - 1 && append_row(a, pol, kt, kt + half_bytes, s, h, hw, j, n_valid - 1);
                 pol.tile(st, a, kt, kt + half_bytes, hw, n_valid, G, scratch);
+                if (patched) fence_proxy_async_smem();  // generic writes before the next TMA fill
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
@@ -449,7 +551,12 @@ __global__ void __launch_bounds__(32 * 16, 1)
                 nparts = 0;
                 for (int c = ca; c <= cb; ++c) nparts += !cta_is_empty(c, W, P);
             }
-            merge_if_last(a, s, h, hw, pair, nparts, ca, cb, W, G);
+            switch (G) {
+                case 1: merge_if_last<1, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
+                case 2: merge_if_last<2, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
+                case 4: merge_if_last<4, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
+                default: merge_if_last<8, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
+            }
         }
         seg = seg_end;
     }

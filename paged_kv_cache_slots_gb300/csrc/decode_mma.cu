@@ -76,6 +76,7 @@ struct MmaPolicy {
     static constexpr bool kTensor = true;
     static constexpr bool kScratch = false;
     static constexpr int KS = D / 16;  // k-steps of QK, m-tiles of PV
+    static constexpr int kD = D;
     using T = typename Elem<DT>::T;
 
     struct State {
@@ -196,6 +197,16 @@ struct MmaPolicy {
             }
         }
         if (n_valid < bs) fence_proxy_async_smem();  // generic writes before the next TMA fill
+    }
+
+    // 16-byte chunk q of row r of head hw's tile (the stage's 128-byte
+    // swizzled layout: chunk c of a row lands at c ^ (row % 8)).
+    __device__ __forceinline__ void patch_chunk(const DecodeArgs& a, uint8_t* t, int hw, int r, int q,
+                                                uint4 val) const {
+        const int bs = a.block_size;
+        const int slice_bytes = a.heads_per_stage * bs * 128;
+        const int row = hw * bs + r;
+        *reinterpret_cast<uint4*>(t + (q >> 3) * slice_bytes + row * 128 + (((q & 7) ^ (row & 7)) << 4)) = val;
     }
 
     // Row sums of heads 2c, 2c+1 over the whole warp.

@@ -371,12 +371,13 @@ kv_status_t paged_decode_workspace_init(void* workspace, size_t workspace_bytes,
     return KV_OK;
 }
 
-kv_status_t paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
-                                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
-                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                   int block_size, kv_dtype_t dtype, float scale, void* out,
-                                   kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
-                                   const kv_decode_options_t* opts, void* stream) {
+static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                               const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, kv_dtype_t dtype, float scale, void* out,
+                               kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                               const kv_decode_options_t* opts, void* stream, const void* k_new,
+                               const void* v_new, const int32_t* append_ids, int32_t* slot_out) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
         return fail(KV_ERR_INVALID_ARG, "paged_decode_attention: sizes out of range");
     if (num_q_heads % num_kv_heads)
@@ -409,6 +410,10 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
         !aligned(workspace, 256))
         return fail(KV_ERR_INVALID_ARG,
                     "alignment: caches, q and out need 16 bytes, the workspace 256 bytes");
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return fail(KV_ERR_INVALID_ARG, "k_new and v_new go together");
+    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16)))
+        return fail(KV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
     int dev = 0, sms = 0, max_smem = 0, smem_sm = 0;
     uint32_t* status = nullptr;
     if (kv_status_t st = device_info(&dev, &status, &sms, &max_smem, &smem_sm)) return st;
@@ -481,6 +486,10 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
     a.pdl = o.no_pdl ? 0 : 1;
     a.test_stall = o.test_stall;
     a.device = dev;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.append_ids = append_ids;
+    a.slot_out = slot_out;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -499,6 +508,33 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
         if (e != cudaSuccess) return cuda_fail(e, "decode reduce launch");
     }
     return KV_OK;
+}
+
+kv_status_t paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, kv_dtype_t dtype, float scale, void* out,
+                                   kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                                   const kv_decode_options_t* opts, void* stream) {
+    return decode_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, dtype, scale, out, out_dtype,
+                       workspace, workspace_bytes, opts, stream, nullptr, nullptr, nullptr, nullptr);
+}
+
+kv_status_t paged_decode_append_attention(const void* q, const void* k_new, const void* v_new,
+                                          const int32_t* seq_ids, void* k_cache, void* v_cache,
+                                          int num_blocks, const int32_t* block_tables, int max_blocks,
+                                          const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                          int num_kv_heads, int head_dim, int block_size,
+                                          kv_dtype_t dtype, float scale, void* out, kv_dtype_t out_dtype,
+                                          int32_t* slot_mapping, void* workspace,
+                                          size_t workspace_bytes, const kv_decode_options_t* opts,
+                                          void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return fail(KV_ERR_INVALID_ARG, "paged_decode_append_attention: null k_new / v_new");
+    return decode_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, dtype, scale, out, out_dtype,
+                       workspace, workspace_bytes, opts, stream, k_new, v_new, seq_ids, slot_mapping);
 }
 
 kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out) {

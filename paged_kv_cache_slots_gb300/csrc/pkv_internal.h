@@ -54,6 +54,12 @@ struct DecodeArgs {
     int32_t* cum;       // [num_seqs + 1]     exclusive prefix of items per sequence
     int32_t* counters;  // [num_seqs * Hkv]   partials merged so far (zero between calls)
     uint32_t* status;
+    // Fused append (paged_decode_append_attention): the new token's rows,
+    // written at position context_lens[s] - 1 and used by this very step.
+    const void* k_new;           // [num_seqs][Hkv][D] or nullptr (no append)
+    const void* v_new;
+    const int32_t* append_ids;   // [num_seqs] or nullptr; a negative entry: no append for s
+    int32_t* slot_out;           // [num_seqs] or nullptr: slot of the newest token
     int num_blocks, max_blocks, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     int dtype, out_dtype;
     float scale_log2;     // scale * log2(e): scores are kept in base-2 units

@@ -56,6 +56,21 @@ def attend(q, kc, vc, tables, ctx, scale, out_dtype=None, **opts):
                                       workspace=ws, **opts)
 
 
+def attend_append(q, kn, vn, kc, vc, tables, ctx, scale, seq_ids=None, out_dtype=None, **opts):
+    """paged_decode_append_attention with poisoned output/workspace; returns (out, slots)."""
+    B, Hq, D = q.shape
+    out_dtype = out_dtype or q.dtype
+    out = torch.full((B, Hq, D), float("nan"), dtype=out_dtype, device=q.device)
+    slots = torch.full((B,), -7, dtype=torch.int32, device=q.device)
+    n = pkv.workspace_bytes(B, Hq, kc.shape[1], D, q.device,
+                            **{k: v for k, v in opts.items() if k != "test_stall"})
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=q.device)
+    pkv.workspace_init(ws, B, kc.shape[1])
+    pkv.paged_decode_append_attention(q, kn, vn, kc, vc, tables, ctx, scale, seq_ids=seq_ids, out=out,
+                                      out_dtype=out_dtype, slot_mapping=slots, workspace=ws, **opts)
+    return out, slots
+
+
 def newest_slot_masks(placement):
     """seq_ids passed to the append: -1 marks a sequence that writes nothing."""
     return np.where(placement.appends, np.arange(len(placement.appends)), -1).astype(np.int32)
@@ -130,16 +145,22 @@ class LargeCase:
         q, kn, vn = step_layer_values(self.spec, len(self.pl.context_lens), layer, self.dev)
         return kc, vc, q, kn, vn
 
-    def check_layer(self, layer, seqs, **opts):
-        """Run one layer on the full batch; compare sampled sequences with the oracle."""
+    def check_layer(self, layer, seqs, fused=False, **opts):
+        """Run one layer on the full batch; compare sampled sequences with the oracle.
+
+        fused: append and attention in one call (paged_decode_append_attention)."""
         s, pl = self.spec, self.pl
         kc, vc, q, kn, vn = self.fill(layer)
         used, ctab = compact_blocks(pl.block_tables, seqs)
         used_t = torch.from_numpy(used.astype(np.int64)).to(self.dev)
         k_pre, v_pre = kc[used_t].cpu(), vc[used_t].cpu()  # the oracle's pool: pre-append
-        slots = pkv.slot_mapping(self.tables, self.ctx, s.block_size, pl.num_blocks)
-        self.pool.append(layer, kn, vn, slots, seq_ids=self.seq_ids)
-        out32 = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, out_dtype=torch.float32, **opts)
+        if fused:
+            out32, slots = attend_append(q, kn, vn, kc, vc, self.tables, self.ctx, s.attn_scale,
+                                         seq_ids=self.seq_ids, out_dtype=torch.float32, **opts)
+        else:
+            slots = pkv.slot_mapping(self.tables, self.ctx, s.block_size, pl.num_blocks)
+            self.pool.append(layer, kn, vn, slots, seq_ids=self.seq_ids)
+            out32 = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, out_dtype=torch.float32, **opts)
         outq = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, **opts)
         st, flags = pkv.device_status()
         assert st == 0 and flags == 0, f"device status {st} flags {flags:#x}"

@@ -12,7 +12,8 @@ import torch
 
 import oracle
 import paged_kv_cache_slots_gb300 as pkv
-from gpu_harness import (LargeCase, SmallCase, attend, bits, check_output, run_step, sample_sequences)
+from gpu_harness import (LargeCase, SmallCase, attend, attend_append, bits, check_output, run_step,
+                         sample_sequences)
 from workloads import SPECS, make_placement, small_spec
 
 pytestmark = pytest.mark.gpu
@@ -46,6 +47,16 @@ def _full_small_check(spec, placement=None, kernels=("auto",), **opts):
         e32 = check_output(out, ref, f"{spec.name}/{kernel} fp32 out")
         eq = check_output(outq, ref, f"{spec.name}/{kernel} {spec.dtype} out")
         errs[kernel] = (e32, eq)
+        # The same step as one fused call on a fresh copy of the pool.
+        d = case.device()
+        out_f, slots_f = attend_append(d["q"], d["kn"], d["vn"], d["kc"], d["vc"], d["tables"], d["ctx"],
+                                       spec.attn_scale, seq_ids=d["seq_ids"], out_dtype=torch.float32,
+                                       kernel=kernel, **opts)
+        assert pkv.device_status() == (0, 0)
+        assert np.array_equal(slots_f.cpu().numpy(), o_slots), "fused slot mapping"
+        assert torch.equal(bits(d["kc"].cpu()), bits(kpost)), "K pool after the fused step"
+        assert torch.equal(bits(d["vc"].cpu()), bits(vpost)), "V pool after the fused step"
+        check_output(out_f, ref, f"{spec.name}/{kernel} fused fp32 out")
     return errs
 
 
@@ -62,8 +73,8 @@ def test_batch32_32_layers_sampled():
     spec = SPECS["llama8b_32l_b32"]
     case = LargeCase(spec, make_placement(spec))
     seqs = sample_sequences(case.pl, 6, seed=20)
-    for layer in (0, spec.num_layers - 1):
-        case.check_layer(layer, seqs)
+    case.check_layer(0, seqs)
+    case.check_layer(spec.num_layers - 1, seqs, fused=True)
     del case
     torch.cuda.empty_cache()
 
@@ -75,7 +86,7 @@ def test_mixed_prefix_b64_sampled():
     # Two whole prefix groups (shared blocks, some members that do not append)
     # plus the longest and shortest sequences.
     seqs = np.unique(np.concatenate([np.arange(0, 8), np.arange(24, 32), sample_sequences(pl, 2, 3)]))
-    case.check_layer(0, seqs)
+    case.check_layer(0, seqs, fused=True)
     # Members of a group that share a table prefix read identical blocks.
     assert (pl.block_tables[0, :8] == pl.block_tables[1, :8]).all()
     del case
@@ -86,8 +97,8 @@ def test_serving_b256_sampled():
     spec = SPECS["serving_b256"]
     case = LargeCase(spec, make_placement(spec))
     seqs = sample_sequences(case.pl, 12, seed=40)
-    for layer in (0, spec.num_layers - 1):
-        case.check_layer(layer, seqs)
+    case.check_layer(0, seqs, fused=True)
+    case.check_layer(spec.num_layers - 1, seqs)
     del case
     torch.cuda.empty_cache()
 
@@ -296,3 +307,36 @@ def test_cuda_graph_capture_of_a_step():
     g.replay()  # appending the same rows again is idempotent
     torch.cuda.synchronize()
     check_output(out, ref, "second replay")
+
+
+def test_cuda_graph_capture_of_a_fused_step():
+    spec = SPECS["llama8b_layer_b8"]
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    o_slots, kpost, vpost, ref = case.oracle()
+    d = case.device()
+    ws = torch.full((pkv.workspace_bytes(8, 32, 8, 128),), 0xFF, dtype=torch.uint8, device="cuda")
+    pkv.workspace_init(ws, 8, 8)
+    out = torch.full((8, 32, 128), float("nan"), dtype=torch.float32, device="cuda")
+    slots = torch.full((8,), -7, dtype=torch.int32, device="cuda")
+
+    def step():
+        pkv.paged_decode_append_attention(d["q"], d["kn"], d["vn"], d["kc"], d["vc"], d["tables"], d["ctx"],
+                                          spec.attn_scale, seq_ids=d["seq_ids"], out=out,
+                                          out_dtype=torch.float32, slot_mapping=slots, workspace=ws)
+
+    step()  # warm-up outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    out.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    check_output(out, ref, "fused graph replay")
+    assert np.array_equal(slots.cpu().numpy(), o_slots)
+    assert torch.equal(bits(d["kc"].cpu()), bits(kpost)) and torch.equal(bits(d["vc"].cpu()), bits(vpost))
