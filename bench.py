@@ -319,7 +319,7 @@ def bench_ours(args, world, rank, local):
     kernel_name = "paged_decode_partial_kernel<MmaPolicy>" if step.kernel != "ffma" else \
         "paged_decode_partial_kernel<FfmaPolicy>"
     if step.fused:
-        kernel_name += " with fused append"
+        kernel_name += "_with_fused_append"
     traffic = recorded_traffic(kernel_name, spec.name)
 
     # End to end through the public API with host buffers (pinned), copies timed.
