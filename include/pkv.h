@@ -255,6 +255,29 @@ kv_status_t paged_decode_append_attention(const void* q, const void* k_new, cons
                                           size_t workspace_bytes, const kv_decode_options_t* opts,
                                           void* stream);
 
+/* paged_decode_attention without a caller-provided workspace, for callers
+ * that cannot allocate device memory (for instance an engine that gave all
+ * free device memory to its KV-block pool at start-up, or code that is handed
+ * only the tensors it works on).  The pages have no counterpart: this is an
+ * interface convenience of this library.
+ *   Scratch: a fixed 8 MiB array in the library's own device memory (held by
+ *   every GPU that loads the library until the process exits); sizes that
+ *   need more (paged_decode_workspace_bytes) are rejected with
+ *   KV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   The first call on a device takes the array's device address (and may
+ *   load the library's device code there): make it before any stream capture.
+ *   Each call clears the array's merge counters on `stream` first.  All calls
+ *   on a device share the array: calls that overlap on the GPU race.
+ * The other arguments and the result are those of paged_decode_attention. */
+kv_status_t paged_decode_attention_static(const void* q, const void* k_cache, const void* v_cache,
+                                          int num_blocks, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, kv_dtype_t dtype,
+                                          float scale, void* out, kv_dtype_t out_dtype,
+                                          const kv_decode_options_t* opts, void* stream);
+
 /* Synchronise `stream`, then read and clear the status word of `device`.
  * flags_out (may be NULL) receives the KV_FLAG_* bits.  Returns KV_OK when no
  * bit was set, KV_ERR_DEVICE_TIMEOUT if the timeout bit was set, else

@@ -79,6 +79,8 @@ def _declare(lib):
         "paged_decode_append_attention": (I, [P, P, P, P, P, P, I, P, I, P, I, I, I, I, I, I,
                                               ctypes.c_float, P, I, P, P, SZ,
                                               ctypes.POINTER(_DecodeOptions), P]),
+        "paged_decode_attention_static": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float,
+                                              P, I, ctypes.POINTER(_DecodeOptions), P]),
         "kv_device_status": (I, [I, P, U32P]),
         "kv_allocator_create": (I, [I, I, I, ctypes.POINTER(P)]),
         "kv_allocator_destroy": (None, [P]),
@@ -319,6 +321,29 @@ def paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, block_table
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
         DTYPE_CODE[q.dtype], float(scale), _ptr(out), DTYPE_CODE[out_dtype], _ptr(slot_mapping),
         _ptr(workspace), workspace.numel(), ctypes.byref(o), _stream(q, stream)), lib)
+    return out
+
+
+def paged_decode_attention_static(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                  out=None, out_dtype=None, stream=None, **opts):
+    """paged_decode_attention with the library's fixed device scratch instead of a
+    workspace: the call allocates nothing (see include/pkv.h)."""
+    lib = load_library()
+    B, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    _need(D == D2 and tuple(v_cache.shape) == tuple(k_cache.shape), "cache shapes")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and the caches share a dtype")
+    _need(all(t.is_contiguous() for t in (q, k_cache, v_cache, block_tables, context_lens)),
+          "contiguous inputs")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32, "int32 tables")
+    out_dtype = out_dtype or q.dtype
+    _need(out is not None, "out must be given (the call allocates nothing)")
+    _need(out.dtype == out_dtype and tuple(out.shape) == (B, Hq, D) and out.is_contiguous(), "out")
+    o = _options(**opts)
+    _check(lib.paged_decode_attention_static(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale), _ptr(out),
+        DTYPE_CODE[out_dtype], ctypes.byref(o), _stream(q, stream)), lib)
     return out
 
 
