@@ -173,6 +173,13 @@ typedef struct {
                             them inside the attention kernel */
     int no_pdl;          /* 1: plain launches; 0: programmatic dependent launch
                             (a kernel's prologue overlaps the previous kernel) */
+    int early_reads;     /* 1: the caller promises that the launch just before
+                            this call on the stream writes neither block_tables,
+                            context_lens nor k_cache/v_cache; the kernel then
+                            reads those (and starts streaming the cache) while
+                            that launch finishes.  q, k_new/v_new, the
+                            workspace and the outputs are still touched only
+                            after it.  Ignored with no_pdl. */
     int test_stall;      /* testing only, 0 in normal use: when non-zero, the
                             producer of CTA 0 stops after one stage so that a
                             consumer's bounded wait (about 2 s) runs out; the

@@ -51,7 +51,7 @@ class _DecodeOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("consumer_warps", ctypes.c_int), ("kernel", ctypes.c_int),
                 ("heads_per_stage", ctypes.c_int), ("separate_reduce", ctypes.c_int),
-                ("no_pdl", ctypes.c_int), ("test_stall", ctypes.c_int)]
+                ("no_pdl", ctypes.c_int), ("early_reads", ctypes.c_int), ("test_stall", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -226,9 +226,9 @@ def slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor, block_s
 
 
 def _options(num_ctas=0, ctas_per_sm=0, consumer_warps=0, kernel="auto", heads_per_stage=0,
-             separate_reduce=False, pdl=True, test_stall=False) -> _DecodeOptions:
+             separate_reduce=False, pdl=True, early_reads=False, test_stall=False) -> _DecodeOptions:
     return _DecodeOptions(num_ctas, ctas_per_sm, consumer_warps, KERNELS[kernel], heads_per_stage,
-                          int(separate_reduce), int(not pdl), int(test_stall))
+                          int(separate_reduce), int(not pdl), int(early_reads), int(test_stall))
 
 
 def workspace_init(workspace: torch.Tensor, num_seqs: int, num_kv_heads: int, stream=None):

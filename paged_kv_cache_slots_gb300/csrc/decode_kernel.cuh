@@ -246,7 +246,6 @@ template <int G, int D>
 __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, int hw, int pair,
                                             int ca, int cb, int64_t W) {
     constexpr int VD = D / 32;
-    constexpr int kParts = 32 / G;  // parts handled per round
     const int lane = threadIdx.x & 31;
     const int Hc = a.heads_per_stage;
     const int64_t P = a.num_ctas;
@@ -455,34 +454,41 @@ __global__ void __launch_bounds__(32 * 16, 1)
             prefetch_tensor_map(&tmv);
         }
     }
-    // Everything above touches only this CTA's shared memory and parameters;
-    // from here on global memory written by the previous launch is read.
-    pdl_wait();
+    // Everything above touches only this CTA's shared memory and parameters.
+    // With early_reads the caller promises that the previous launch on the
+    // stream writes neither the tables, the lengths nor the K/V cache, so the
+    // prefix, the table entries and the first stages are fetched while that
+    // launch finishes; everything else (q, the new rows, the workspace, the
+    // outputs) is touched only after waiting for it.
+    if (!a.early_reads) pdl_wait();
     build_prefix(a, chunks, cum, scan);  // ends with __syncthreads
     const int64_t W = cum[a.num_seqs];
     const int P = a.num_ctas;
-    if (blockIdx.x == 0 && !a.fused_reduce) {
-        for (int s = tid; s <= a.num_seqs; s += blockDim.x) a.cum[s] = cum[s];
-    }
-    // Sequences with no tokens: zero rows (fused merge) and slot -1 (CTA s mod P).
-    for (int s = blockIdx.x; s < a.num_seqs; s += P) {
-        if (cum[s + 1] != cum[s]) continue;
-        if (a.slot_out && tid == 0) a.slot_out[s] = -1;
-        if (!a.fused_reduce) continue;
-        const int64_t o0 = static_cast<int64_t>(s) * a.num_q_heads * D;
-        for (int e = tid; e < a.num_q_heads * D; e += blockDim.x)
-            store_out(a.out, o0 + e, 0.f, a.out_dtype);
-    }
     const int start = static_cast<int>(static_cast<int64_t>(blockIdx.x) * W / P);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x) + 1) * W / P);
-    if (start >= end) return;
-
     const int warp = tid >> 5, lane = tid & 31;
-    if (warp == 0) {
+    if (warp == 0 && start < end) {
         produce<Policy::kTensor>(a, ring, full, empty, cum, chunks, start, end, half_bytes, &tmk,
                                  &tmv, abort);
         return;
     }
+    if (a.early_reads) pdl_wait();
+    // Global writes of the prologue, by the threads that are not producing.
+    const int wt = start < end ? tid - 32 : tid;
+    const int nwt = start < end ? static_cast<int>(blockDim.x) - 32 : static_cast<int>(blockDim.x);
+    if (blockIdx.x == 0 && !a.fused_reduce) {
+        for (int s = wt; s <= a.num_seqs; s += nwt) a.cum[s] = cum[s];
+    }
+    // Sequences with no tokens: zero rows (fused merge) and slot -1 (CTA s mod P).
+    for (int s = blockIdx.x; s < a.num_seqs; s += P) {
+        if (cum[s + 1] != cum[s]) continue;
+        if (a.slot_out && wt == 0) a.slot_out[s] = -1;
+        if (!a.fused_reduce) continue;
+        const int64_t o0 = static_cast<int64_t>(s) * a.num_q_heads * D;
+        for (int e = wt; e < a.num_q_heads * D; e += nwt) store_out(a.out, o0 + e, 0.f, a.out_dtype);
+    }
+    if (start >= end) return;
+
     const int w = warp - 1;
     const int hw = w % Hc;  // head within the chunk
     const int rr = w / Hc;  // replica among the R warps of that head

@@ -95,11 +95,11 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Options {
     int num_ctas, ctas_per_sm, consumer_warps, kernel, heads_per_stage, separate_reduce, no_pdl,
-        test_stall;
+        early_reads, test_stall;
 };
 
 kv_status_t read_options(const kv_decode_options_t* o, Options* out) {
-    Options r{0, 1, 0, KV_KERNEL_AUTO, 0, 0, 0, 0};
+    Options r{0, 1, 0, KV_KERNEL_AUTO, 0, 0, 0, 0, 0};
     if (o) {
         if (o->num_ctas < 0 || o->ctas_per_sm < 0 || o->consumer_warps < 0 ||
             o->consumer_warps > 15 || o->ctas_per_sm > 8 || o->heads_per_stage < 0 ||
@@ -114,6 +114,7 @@ kv_status_t read_options(const kv_decode_options_t* o, Options* out) {
         r.heads_per_stage = o->heads_per_stage;
         r.separate_reduce = o->separate_reduce != 0;
         r.no_pdl = o->no_pdl != 0;
+        r.early_reads = o->early_reads != 0;
         r.test_stall = o->test_stall != 0;
     }
     *out = r;
@@ -484,6 +485,7 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     a.smem_bytes = plan.smem_bytes;
     a.fused_reduce = o.separate_reduce ? 0 : 1;
     a.pdl = o.no_pdl ? 0 : 1;
+    a.early_reads = (o.early_reads && !o.no_pdl) ? 1 : 0;
     a.test_stall = o.test_stall;
     a.device = dev;
     a.k_new = k_new;

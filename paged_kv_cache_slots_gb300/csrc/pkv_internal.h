@@ -71,6 +71,7 @@ struct DecodeArgs {
     int smem_bytes;
     int fused_reduce;     // 1: the last CTA of a split pair merges it (no reduce kernel)
     int pdl;              // 1: launch with programmatic dependent launch
+    int early_reads;      // 1: tables, lengths and cache may be read before the previous launch ends
     int test_stall;       // testing only: see kv_decode_options_t
     int device;           // CUDA ordinal the launch targets
 };

@@ -74,7 +74,7 @@ def test_batch32_32_layers_sampled():
     case = LargeCase(spec, make_placement(spec))
     seqs = sample_sequences(case.pl, 6, seed=20)
     case.check_layer(0, seqs)
-    case.check_layer(spec.num_layers - 1, seqs, fused=True)
+    case.check_layer(spec.num_layers - 1, seqs, fused=True, early_reads=True)
     del case
     torch.cuda.empty_cache()
 
@@ -97,7 +97,7 @@ def test_serving_b256_sampled():
     spec = SPECS["serving_b256"]
     case = LargeCase(spec, make_placement(spec))
     seqs = sample_sequences(case.pl, 12, seed=40)
-    case.check_layer(0, seqs, fused=True)
+    case.check_layer(0, seqs, fused=True, early_reads=True)
     case.check_layer(spec.num_layers - 1, seqs)
     del case
     torch.cuda.empty_cache()
@@ -135,7 +135,8 @@ SPLITS = [dict(), dict(num_ctas=1, consumer_warps=8), dict(num_ctas=2, consumer_
           dict(num_ctas=7, consumer_warps=3), dict(num_ctas=64), dict(num_ctas=1000, consumer_warps=15),
           dict(num_ctas=152, consumer_warps=4), dict(heads_per_stage=1), dict(heads_per_stage=2),
           dict(heads_per_stage=4, consumer_warps=12), dict(separate_reduce=True),
-          dict(separate_reduce=True, num_ctas=1000), dict(pdl=False), dict(ctas_per_sm=2)]
+          dict(separate_reduce=True, num_ctas=1000), dict(pdl=False), dict(ctas_per_sm=2),
+          dict(early_reads=True), dict(early_reads=True, num_ctas=1000, separate_reduce=True)]
 
 
 @pytest.mark.parametrize("kernel", ["mma", "ffma"])
