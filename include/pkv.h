@@ -318,6 +318,51 @@ kv_status_t kv_allocator_slot(const kv_block_allocator_t* a, int64_t seq_id, int
 kv_status_t kv_allocator_free_queue(const kv_block_allocator_t* a, int32_t* out, int capacity,
                                     int* count_out);
 
+/* ------------------------------------------ block pool with prefix caching */
+
+/* The block pool of "Reading Inference Engine Codebases", Examples 12 and 13
+ * (vLLM's KV cache manager and block pool), host side, single-threaded.
+ *
+ * Every full block of a request is indexed by a chained hash of its parent's
+ * hash and its own token ids, so it names the whole prefix up to its end.
+ * kv_prefix_pool_allocate(tokens) takes:
+ *   1. the longest run of cached full blocks matching the request's prefix,
+ *      at most (num_tokens - 1) / block_size blocks (the last token is always
+ *      computed again); each hit gains a reference and leaves the free queue;
+ *   2. ceil(num_tokens / block_size) minus the hits new blocks from the front
+ *      of the free queue; a popped block that still has a hash loses it
+ *      (eviction, reported in evicted_out); each new full block is cached
+ *      under its prefix hash, with no de-duplication of equal blocks.
+ * kv_prefix_pool_free(blocks) drops one reference per block, walking the list
+ * tail first; a block reaching zero goes to the front of the free queue when
+ * it has no hash, to the back when it has one (least recently used first).
+ * The free queue starts as all blocks in increasing id order.
+ *
+ * tokens: host int32[num_tokens], any values.  blocks_out: host, capacity
+ * entries, receives the request's blocks in table order.  cached_tokens_out
+ * (may be NULL): hit blocks x block_size.  evicted_out (may be NULL) receives
+ * up to evicted_capacity evicted block ids in eviction order;
+ * num_evicted_out (may be NULL) the count.  When fewer blocks are free than
+ * the request needs, KV_ERR_OUT_OF_BLOCKS and nothing changes.  Freeing a
+ * block whose count is already zero, or an id out of range, is
+ * KV_ERR_INVALID_ARG and nothing changes. */
+typedef struct kv_prefix_pool kv_prefix_pool_t;
+
+kv_status_t kv_prefix_pool_create(int num_blocks, int block_size, kv_prefix_pool_t** out);
+void kv_prefix_pool_destroy(kv_prefix_pool_t* p);
+kv_status_t kv_prefix_pool_allocate(kv_prefix_pool_t* p, const int32_t* tokens, int num_tokens,
+                                    int32_t* blocks_out, int capacity, int* num_blocks_out,
+                                    int* cached_tokens_out, int32_t* evicted_out,
+                                    int evicted_capacity, int* num_evicted_out);
+kv_status_t kv_prefix_pool_free(kv_prefix_pool_t* p, const int32_t* blocks, int n);
+/* The free queue, front (next to be reused) first.  With out == NULL only
+ * count_out is written. */
+kv_status_t kv_prefix_pool_free_queue(const kv_prefix_pool_t* p, int32_t* out, int capacity,
+                                      int* count_out);
+/* Number of distinct cached prefix hashes and of blocks holding one. */
+kv_status_t kv_prefix_pool_cache_size(const kv_prefix_pool_t* p, int* hashes_out,
+                                      int* blocks_out);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

@@ -17,7 +17,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "KVError", "KVPool", "BlockAllocator", "kv_pool_bytes", "slot_mapping", "workspace_bytes",
+    "KVError", "KVPool", "BlockAllocator", "PrefixCachePool", "kv_pool_bytes", "slot_mapping", "workspace_bytes",
     "paged_decode_attention", "device_status", "library_path", "load_library", "workspace_init",
     "make_workspace", "paged_decode_append_attention",
 ]
@@ -90,6 +90,15 @@ def _declare(lib):
                                    ctypes.POINTER(I), ctypes.POINTER(I)]),
         "kv_allocator_slot": (I, [P, I64, I, ctypes.POINTER(ctypes.c_int32)]),
         "kv_allocator_free_queue": (I, [P, ctypes.POINTER(ctypes.c_int32), I, ctypes.POINTER(I)]),
+        "kv_prefix_pool_create": (I, [I, I, ctypes.POINTER(P)]),
+        "kv_prefix_pool_destroy": (None, [P]),
+        "kv_prefix_pool_allocate": (I, [P, ctypes.POINTER(ctypes.c_int32), I,
+                                        ctypes.POINTER(ctypes.c_int32), I, ctypes.POINTER(I),
+                                        ctypes.POINTER(I), ctypes.POINTER(ctypes.c_int32), I,
+                                        ctypes.POINTER(I)]),
+        "kv_prefix_pool_free": (I, [P, ctypes.POINTER(ctypes.c_int32), I]),
+        "kv_prefix_pool_free_queue": (I, [P, ctypes.POINTER(ctypes.c_int32), I, ctypes.POINTER(I)]),
+        "kv_prefix_pool_cache_size": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -405,6 +414,62 @@ class BlockAllocator:
         try:
             if getattr(self, "_h", None):
                 self._lib.kv_allocator_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+
+class PrefixCachePool:
+    """Host block pool with prefix caching (chained block hashes, LRU free queue)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check(self._lib.kv_prefix_pool_create(num_blocks, block_size, ctypes.byref(h)), self._lib)
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def allocate(self, tokens):
+        """Blocks for a request with these token ids: (blocks, cached_tokens, evicted).
+
+        Returns None (nothing changed) when too few blocks are free."""
+        tokens = [int(t) for t in tokens]
+        n = len(tokens)
+        cap = max(1, -(-n // self.block_size))
+        tok = (ctypes.c_int32 * max(1, n))(*tokens)
+        blocks = (ctypes.c_int32 * cap)()
+        evicted = (ctypes.c_int32 * cap)()
+        nb, cached, ne = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        st = self._lib.kv_prefix_pool_allocate(self._h, tok, n, blocks, cap, ctypes.byref(nb),
+                                               ctypes.byref(cached), evicted, cap, ctypes.byref(ne))
+        if st == 4:  # KV_ERR_OUT_OF_BLOCKS
+            return None
+        _check(st, self._lib)
+        return list(blocks[:nb.value]), int(cached.value), list(evicted[:ne.value])
+
+    def free(self, blocks):
+        blocks = [int(b) for b in blocks]
+        buf = (ctypes.c_int32 * max(1, len(blocks)))(*blocks)
+        _check(self._lib.kv_prefix_pool_free(self._h, buf, len(blocks)), self._lib)
+
+    def free_queue(self):
+        n = ctypes.c_int()
+        _check(self._lib.kv_prefix_pool_free_queue(self._h, None, 0, ctypes.byref(n)), self._lib)
+        buf = (ctypes.c_int32 * max(1, n.value))()
+        _check(self._lib.kv_prefix_pool_free_queue(self._h, buf, n.value, None), self._lib)
+        return list(buf[:n.value])
+
+    def cache_size(self):
+        h, b = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.kv_prefix_pool_cache_size(self._h, ctypes.byref(h), ctypes.byref(b)),
+               self._lib)
+        return int(h.value), int(b.value)
+
+    def __del__(self):
+        try:
+            if getattr(self, "_h", None):
+                self._lib.kv_prefix_pool_destroy(self._h)
                 self._h = None
         except Exception:
             pass

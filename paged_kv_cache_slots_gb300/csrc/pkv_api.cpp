@@ -189,6 +189,14 @@ kv_status_t encode_cache_map(CUtensorMap* map, const void* base, int dtype, int 
 
 }  // namespace
 
+kv_status_t pkv::report_error(kv_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
 // ------------------------------------------------------------------ pool
 struct kv_pool {
     kv_pool_config_t cfg;

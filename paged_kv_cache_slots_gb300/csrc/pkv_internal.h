@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "pkv.h"
+
 namespace pkv {
 
 // Element types as stored in the pool, q and out (same codes as kv_dtype_t).
@@ -98,5 +100,9 @@ int max_dynamic_smem(int device);
 
 // Device address of the current device's status word.
 cudaError_t status_word_address(uint32_t** ptr);
+
+// Records a printf-style message for kv_last_error() on this thread and
+// returns st.
+kv_status_t report_error(kv_status_t st, const char* fmt, ...);
 
 }  // namespace pkv

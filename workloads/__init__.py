@@ -269,3 +269,32 @@ def small_spec(name="custom", *, num_q_heads=4, num_kv_heads=2, head_dim=64,
                         num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size,
                         dtype=dtype, seed=seed, ctx_dist="list", ctx_list=ctx,
                         num_blocks=num_blocks or max(1, 2 * need), scale=scale)
+
+
+def prefix_request_trace(seed: int, num_ops: int, *, num_prompts: int = 6, vocab: int = 50,
+                         max_shared: int = 40, max_own: int = 24, free_prob: float = 0.45):
+    """A seeded stream of request arrivals and departures for a prefix-caching
+    block pool: ("allocate", tokens) and ("free", index of an earlier live
+    allocation, counted in arrival order).  Requests draw one of `num_prompts`
+    shared prompts (some of it, all of it, or none) and append their own
+    random tokens, so hits, partial hits, exact repeats and misses all occur.
+    Token ids are small so that equal blocks in unrelated positions occur too.
+    """
+    rng = np.random.default_rng(seed)
+    prompts = [rng.integers(0, vocab, size=max_shared).tolist() for _ in range(num_prompts)]
+    ops = []
+    live = 0
+    for _ in range(num_ops):
+        if live and rng.random() < free_prob:
+            ops.append(("free", int(rng.integers(0, live))))
+            live -= 1
+            continue
+        p = prompts[int(rng.integers(0, num_prompts))]
+        shared = int(rng.choice([0, int(rng.integers(1, max_shared + 1)), max_shared]))
+        own = int(rng.integers(0, max_own + 1))
+        tokens = p[:shared] + rng.integers(0, vocab, size=own).tolist()
+        if not tokens:
+            tokens = [int(rng.integers(0, vocab))]
+        ops.append(("allocate", tokens))
+        live += 1
+    return ops
