@@ -63,6 +63,10 @@ def parse_args():
                    help="slot mapping + append + attention as separate calls instead of one fused call per layer")
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: run the first N layers (the JSON line then names N)")
+    p.add_argument("--swap", action="store_true",
+                   help="measure swap-out/in of KV blocks to page-locked host memory instead")
+    p.add_argument("--swap-requests", type=int, default=8,
+                   help="requests of 2000 tokens (8B shape) swapped per timed copy")
     p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -495,6 +499,94 @@ def bench_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- swap leg
+def bench_swap(args, world, rank, local):
+    """Swap-out and swap-in throughput of whole KV blocks (every layer's K and V)
+    between the pool and page-locked host memory, for the preempted request of
+    "Batching and Scheduling", Example 8: 2000 tokens of the 8B shape (125
+    blocks of 16 tokens, 32 layers, 8 KV heads, head_dim 128, bf16), i.e.
+    250 MiB each way, `--swap-requests` such requests per copy.  The link's
+    own ceiling is measured beside it: one contiguous cudaMemcpyAsync of the
+    same byte count each way through the copy engines."""
+    import paged_kv_cache_slots_gb300 as pkv
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, True)
+    per_req = 125
+    nreq = max(1, args.swap_requests)
+    nblk = per_req * nreq
+    pool = pkv.KVPool(32, 2 * nblk + 16, 16, 8, 128, torch.bfloat16, device=device)
+    pool.buffer.view(torch.int16).random_(generator=torch.Generator(device=device).manual_seed(5))
+    perm = torch.randperm(2 * nblk + 16, generator=torch.Generator().manual_seed(9))
+    ids = perm[:nblk].to(torch.int32).to(device)
+    nbytes = pool.swap_bytes(nblk)
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev_copy = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def timed(fn, reps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1) / reps, world, device)
+
+    reps = max(1, min(args.steps, 50))
+    with ClockSampler(local) as clocks:
+        out_ms = timed(lambda: pool.swap_out(ids, host=host), reps)
+        in_ms = timed(lambda: pool.swap_in(ids, host), reps)
+        ce_out_ms = timed(lambda: host.copy_(dev_copy, non_blocking=True), reps)
+        ce_in_ms = timed(lambda: dev_copy.copy_(host, non_blocking=True), reps)
+    # The copies above are checked, not only timed: the pool must round-trip.
+    before = pool.buffer.clone()
+    pool.swap_out(ids, host=host)
+    for layer in (0, 31):
+        for t in pool.layer(layer):
+            t[ids.long()] = 0
+    pool.swap_in(ids, host)
+    torch.cuda.synchronize()
+    blocks_ok = bool(torch.equal(pool.buffer, before))
+    status, flags = pkv.device_status(device)
+    if rank != 0:
+        return
+    gbs = lambda ms: nbytes * world / (ms * 1e-3) / 1e9  # noqa: E731
+    page_bytes = pool.swap_bytes(per_req)
+    line = {
+        "metric": "KV swap GB/s (host memory, out and back)",
+        "value": round(2 * nbytes * world / ((out_ms + in_ms) * 1e-3) / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": reps,
+        "warmup": max(3, args.warmup),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"swap {nreq} x 2000-token 8B-shaped requests "
+                               f"({nblk} blocks, {nbytes / 2**20:.0f} MiB each way)",
+                   "host_memory": "page-locked", "l2": "inputs larger than L2"},
+        "swap_out_gbs": round(gbs(out_ms), 1),
+        "swap_in_gbs": round(gbs(in_ms), 1),
+        "copy_engine_d2h_gbs": round(gbs(ce_out_ms), 1),
+        "copy_engine_h2d_gbs": round(gbs(ce_in_ms), 1),
+        "page_request_out_and_back_ms": round((out_ms + in_ms) * page_bytes / nbytes, 3),
+        "page_request_pcie4_ms": round(2 * page_bytes / 31.5e9 * 1e3, 1),
+        "round_trip_exact": blocks_ok,
+        "device_status": [status, flags],
+        "gpu_launches": 2 * reps,
+        "clocks": clocks.summary(),
+        "vs_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
@@ -503,6 +595,9 @@ def main():
         return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    if args.swap:
+        bench_swap(args, world, rank, local)
+        return
     bench_ours(args, world, rank, local)
 
 

@@ -291,6 +291,38 @@ kv_status_t paged_decode_attention_static(const void* q, const void* k_cache, co
  * KV_ERR_DEVICE_CHECK. */
 kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out);
 
+/* ------------------------------------------------------ swap to host memory */
+
+/* Preemption by swap ("Batching and Scheduling", Example 8): a request's KV
+ * blocks are copied to CPU memory and later copied back, instead of being
+ * dropped and computed again.
+ *
+ * A swapped block is all of one physical block across the pool: every layer's
+ * K and V rows.  Host record layout, for block i of the list:
+ *   [i][2 * num_layers][num_kv_heads][block_size][head_dim] elements,
+ * unit 2*l holding layer l's K rows and unit 2*l + 1 its V rows, each in the
+ * pool's own [Hkv][bs][D] order.  kv_swap_bytes(pool, n) is the size of n
+ * records: n * 2 * num_layers * num_kv_heads * block_size * head_dim * elem.
+ *
+ * kv_swap_out copies pool blocks block_ids[0..n) to records 0..n of host_dst;
+ * kv_swap_in copies records 0..n of host_src into pool blocks block_ids[0..n)
+ * (which need not be the blocks they came from).  One kernel each, enqueued
+ * on `stream`; the GPU reads and writes the host buffer directly, so it must
+ * be memory the device addresses: page-locked host memory (cudaHostAlloc,
+ * cudaHostRegister), managed memory or device memory, 16-byte aligned, at
+ * least kv_swap_bytes(pool, n) bytes.  block_ids: int32[n], device-addressable
+ * likewise.  Pageable host memory is refused with KV_ERR_INVALID_ARG.
+ * Ownership stays with the caller; the host buffer must stay alive and
+ * untouched by the CPU until the stream reaches the copy's end.
+ * Block ids outside [0, num_blocks) are skipped and set
+ * KV_FLAG_BAD_BLOCK_ID in the device status word.  Swap-in with a block id
+ * listed twice leaves that block holding either record. */
+size_t kv_swap_bytes(const kv_pool_t* pool, int num_blocks);
+kv_status_t kv_swap_out(const kv_pool_t* pool, const int32_t* block_ids, int n, void* host_dst,
+                        size_t host_bytes, void* stream);
+kv_status_t kv_swap_in(kv_pool_t* pool, const int32_t* block_ids, int n, const void* host_src,
+                       size_t host_bytes, void* stream);
+
 /* --------------------------------------------------- host block allocator */
 
 /* A host-side allocator of physical blocks, the bookkeeping that produces the

@@ -90,6 +90,9 @@ def _declare(lib):
                                    ctypes.POINTER(I), ctypes.POINTER(I)]),
         "kv_allocator_slot": (I, [P, I64, I, ctypes.POINTER(ctypes.c_int32)]),
         "kv_allocator_free_queue": (I, [P, ctypes.POINTER(ctypes.c_int32), I, ctypes.POINTER(I)]),
+        "kv_swap_bytes": (SZ, [P, I]),
+        "kv_swap_out": (I, [P, P, I, P, SZ, P]),
+        "kv_swap_in": (I, [P, P, I, P, SZ, P]),
         "kv_prefix_pool_create": (I, [I, I, ctypes.POINTER(P)]),
         "kv_prefix_pool_destroy": (None, [P]),
         "kv_prefix_pool_allocate": (I, [P, ctypes.POINTER(ctypes.c_int32), I,
@@ -193,6 +196,43 @@ class KVPool:
             off = addr - base
             views.append(self.buffer[off:off + n].view(self.dtype).view(self.shape))
         return views[0], views[1]
+
+    def swap_bytes(self, num_blocks: int) -> int:
+        """Bytes of host memory that num_blocks swapped blocks occupy."""
+        return int(self._lib.kv_swap_bytes(self._handle, num_blocks))
+
+    def _swap_ids(self, block_ids) -> torch.Tensor:
+        if not isinstance(block_ids, torch.Tensor):
+            block_ids = torch.tensor(list(block_ids), dtype=torch.int32)
+        _need(block_ids.dtype == torch.int32 and block_ids.dim() == 1, "block_ids must be int32 [n]")
+        return block_ids.to(self.device).contiguous()
+
+    def swap_out(self, block_ids, host: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Copy the listed blocks (all layers, K and V) into page-locked host memory.
+
+        Returns the host buffer (uint8, kv_swap_bytes(n) bytes; a new pinned
+        tensor unless `host` is given).  Asynchronous on `stream`."""
+        ids = self._swap_ids(block_ids)
+        n = ids.numel()
+        need = self.swap_bytes(n)
+        if host is None:
+            host = torch.empty(max(need, 16), dtype=torch.uint8, pin_memory=True)
+        _need(host.dtype == torch.uint8 and host.is_contiguous() and host.numel() >= need,
+              "host must be a contiguous uint8 tensor of at least swap_bytes(n) bytes")
+        _check(self._lib.kv_swap_out(self._handle, _ptr(ids), n, _ptr(host), host.numel(),
+                                     _stream(self.buffer, stream)), self._lib)
+        self._swap_keep = ids  # alive until the next swap call on this pool
+        return host
+
+    def swap_in(self, block_ids, host: torch.Tensor, stream=None):
+        """Copy swapped records from host memory into the listed blocks."""
+        ids = self._swap_ids(block_ids)
+        n = ids.numel()
+        _need(host.dtype == torch.uint8 and host.is_contiguous() and host.numel() >= self.swap_bytes(n),
+              "host must be a contiguous uint8 tensor of at least swap_bytes(n) bytes")
+        _check(self._lib.kv_swap_in(self._handle, _ptr(ids), n, _ptr(host), host.numel(),
+                                    _stream(self.buffer, stream)), self._lib)
+        self._swap_keep = ids
 
     def append(self, layer: int, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                seq_ids: torch.Tensor | None = None, stream=None):

@@ -216,6 +216,66 @@ struct kv_block_allocator {
     std::unordered_map<int64_t, Seq> seqs;
 };
 
+namespace {
+
+// Moves blocks between the pool and a buffer the GPU can address.
+kv_status_t swap_blocks(kv_pool_t* p, const int32_t* block_ids, int n, void* host,
+                        size_t host_bytes, bool to_host, void* stream) {
+    const char* what = to_host ? "kv_swap_out" : "kv_swap_in";
+    if (!p) return fail(KV_ERR_INVALID_ARG, "%s: null pool", what);
+    if (n < 0) return fail(KV_ERR_INVALID_ARG, "%s: %d blocks", what, n);
+    if (n == 0) return KV_OK;
+    if (!block_ids || !host) return fail(KV_ERR_INVALID_ARG, "%s: null pointer", what);
+    const size_t need = kv_swap_bytes(p, n);
+    if (host_bytes < need)
+        return fail(KV_ERR_INVALID_ARG, "%s: host buffer of %zu bytes < %zu needed", what,
+                    host_bytes, need);
+    if (!aligned(host, 16)) return fail(KV_ERR_INVALID_ARG, "%s: host buffer must be 16-byte aligned", what);
+    DeviceGuard g(p->cfg.device);
+    if (!g.ok) return fail(KV_ERR_CUDA, "cannot select device %d", p->cfg.device);
+    // The kernel dereferences both pointers: they must be memory the GPU
+    // addresses (page-locked or registered host memory, managed or device
+    // memory), not plain pageable memory.
+    void* dev_ptrs[2] = {host, const_cast<int32_t*>(block_ids)};
+    for (int k = 0; k < 2; ++k) {
+        cudaPointerAttributes attr{};
+        cudaError_t e = cudaPointerGetAttributes(&attr, dev_ptrs[k]);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return cuda_fail(e, "cudaPointerGetAttributes");
+        }
+        if (attr.type == cudaMemoryTypeUnregistered)
+            return fail(KV_ERR_INVALID_ARG,
+                        "%s: %s is pageable host memory; use page-locked (cudaHostAlloc / "
+                        "cudaHostRegister), managed or device memory", what,
+                        k == 0 ? "the host buffer" : "block_ids");
+        if (attr.type == cudaMemoryTypeHost) {
+            if (!attr.devicePointer)
+                return fail(KV_ERR_INVALID_ARG, "%s: host memory not mapped for the device", what);
+            dev_ptrs[k] = attr.devicePointer;
+        }
+    }
+    uint32_t* status = nullptr;
+    int sms = 0;
+    if (kv_status_t st = device_info(nullptr, &status, &sms, nullptr, nullptr)) return st;
+    SwapArgs a{p->base,
+               static_cast<char*>(dev_ptrs[0]),
+               static_cast<const int32_t*>(dev_ptrs[1]),
+               status,
+               static_cast<int64_t>(p->layer_bytes),
+               static_cast<int64_t>(p->layer_bytes / p->cfg.num_blocks),
+               n,
+               p->cfg.num_layers,
+               p->cfg.num_blocks,
+               to_host ? 1 : 0,
+               1};
+    cudaError_t e = launch_swap(a, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "swap launch");
+    return KV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* kv_status_string(kv_status_t s) {
@@ -349,6 +409,22 @@ kv_status_t kv_append(kv_pool_t* p, int layer, const int32_t* seq_ids, int n_tok
     cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return KV_OK;
+}
+
+size_t kv_swap_bytes(const kv_pool_t* p, int num_blocks) {
+    if (!p || num_blocks < 0) return 0;
+    return static_cast<size_t>(num_blocks) * 2 * p->layer_bytes / p->cfg.num_blocks *
+           p->cfg.num_layers;
+}
+
+kv_status_t kv_swap_out(const kv_pool_t* p, const int32_t* block_ids, int n, void* host_dst,
+                        size_t host_bytes, void* stream) {
+    return swap_blocks(const_cast<kv_pool_t*>(p), block_ids, n, host_dst, host_bytes, true, stream);
+}
+
+kv_status_t kv_swap_in(kv_pool_t* p, const int32_t* block_ids, int n, const void* host_src,
+                       size_t host_bytes, void* stream) {
+    return swap_blocks(p, block_ids, n, const_cast<void*>(host_src), host_bytes, false, stream);
 }
 
 kv_status_t paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

@@ -28,6 +28,19 @@ struct AppendArgs {
     int pdl;
 };
 
+// Block swap between the pool and a device-addressable host buffer.
+struct SwapArgs {
+    char* pool;               // pool base: layer l's K at 2l * layer_bytes, V at (2l + 1) * layer_bytes
+    char* host;               // [n][2 * num_layers][unit_bytes]
+    const int32_t* block_ids;  // [n] physical blocks
+    uint32_t* status;
+    int64_t layer_bytes;      // one of K or V of one layer
+    int64_t unit_bytes;       // one block of one of K or V of one layer (multiple of 16)
+    int n, num_layers, num_blocks;
+    int to_host;              // 1: pool -> host (swap out), 0: host -> pool (swap in)
+    int pdl;
+};
+
 struct SlotArgs {
     const int32_t* block_tables;
     const int32_t* context_lens;
@@ -90,6 +103,7 @@ bool decode_plan(int kernel, int dtype, int head_dim, int block_size, int group,
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_slot_mapping(const SlotArgs& a, cudaStream_t stream);
+cudaError_t launch_swap(const SwapArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_ffma(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& tmap_k,
                               const CUtensorMap& tmap_v, cudaStream_t stream);
