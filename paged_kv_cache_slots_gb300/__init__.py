@@ -25,6 +25,7 @@ __all__ = [
 KV_F32, KV_F16, KV_BF16 = 0, 1, 2
 DTYPE_CODE = {torch.float32: KV_F32, torch.float16: KV_F16, torch.bfloat16: KV_BF16}
 CODE_DTYPE = {v: k for k, v in DTYPE_CODE.items()}
+DTYPE_NAMES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 KERNELS = {"auto": 0, "ffma": 1, "mma": 2}
 FLAG_BAD_BLOCK_ID, FLAG_BAD_SLOT, FLAG_BAD_CONTEXT, FLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
@@ -161,6 +162,9 @@ class KVPool:
         device = torch.device(device if device is not None else "cuda")
         if device.index is None:
             device = torch.device("cuda", torch.cuda.current_device())
+        if isinstance(dtype, str):
+            _need(dtype in DTYPE_NAMES, f"dtype must be one of {sorted(DTYPE_NAMES)}")
+            dtype = DTYPE_NAMES[dtype]
         self.cfg = _PoolConfig(num_layers, num_blocks, block_size, num_kv_heads, head_dim,
                                DTYPE_CODE[dtype], device.index)
         self.nbytes = int(lib.kv_pool_bytes(ctypes.byref(self.cfg)))
