@@ -27,6 +27,17 @@
  * Attention is the plain definition: gather the sequence's K and V through
  * the table into contiguous fp64 arrays, then dense softmax attention with
  * the maximum subtracted before exp.
+ *
+ * FP8 KV cache ("vLLM Architecture and Installation", Example 6, startup
+ * memory profiling and the number of KV blocks: with an FP8 KV cache each
+ * value takes one byte instead of two, so blocks halve and the token
+ * capacity doubles).  The pages name
+ * the 8-bit format but not its layout or scaling; the plain reading taken
+ * here is E4M3 (sign, 4-bit exponent with bias 7, 3-bit fraction, no
+ * infinities, S.1111.111 is NaN, largest finite 448) with one fp32 scale per
+ * layer for K and one for V: a stored byte b stands for scale * e4m3(b), and
+ * a value x is stored as the code nearest to the fp32 quotient x / scale
+ * (ties to the even code, magnitudes from 448 up saturating to 448).
  */
 #include <math.h>
 #include <pthread.h>
@@ -35,9 +46,53 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3 };
 
-static size_t orc_elem_bytes(int dtype) { return dtype == ORC_F32 ? 4u : 2u; }
+static size_t orc_elem_bytes(int dtype) {
+    return dtype == ORC_F32 ? 4u : dtype == ORC_E4M3 ? 1u : 2u;
+}
+
+/* E4M3 -> double, from the format's definition: sign | 4-bit exponent
+ * (bias 7) | 3-bit fraction; exponent 0 holds subnormals frac * 2^-9;
+ * exponent 15 with fraction 7 is NaN (there is no infinity). */
+static double orc_e4m3_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int expo = (b >> 3) & 0xf;
+    int frac = b & 0x7;
+    double v;
+    if (expo == 15 && frac == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)frac, -9);
+    else
+        v = ldexp((double)(8 + frac), expo - 10); /* 1.frac * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code of a binary32 value, by search over every finite code:
+ * the code whose value is closest to x, the even code (fraction LSB 0) on a
+ * tie, magnitudes at or above the largest finite value (448) saturate to it,
+ * NaN gives 0x7F, the sign is kept (also for zero). */
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7e;
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7e; ++c) {
+        double err = fabs(orc_e4m3_to_double((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+/* Quantize n stored values of src_dtype with one scale: the fp32 quotient
+ * x / scale, then the nearest code. */
+void oracle_quantize_e4m3(int src_dtype, const void* src, int64_t n, float scale, uint8_t* out);
 
 /* IEEE binary16 -> double, written from the format's definition:
  * sign | 5-bit exponent (bias 15) | 10-bit fraction. */
@@ -64,6 +119,7 @@ static double orc_bf16_to_double(uint16_t b) {
 }
 
 static double orc_load(const void* base, size_t idx, int dtype) {
+    if (dtype == ORC_E4M3) return orc_e4m3_to_double(((const uint8_t*)base)[idx]);
     if (dtype == ORC_F32) {
         float f;
         memcpy(&f, (const char*)base + 4 * idx, 4);
@@ -77,6 +133,14 @@ static double orc_load(const void* base, size_t idx, int dtype) {
 /* Decode n stored values to double (exposed so tests can pin the decoders). */
 void oracle_decode(int dtype, const void* src, int64_t n, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_load(src, (size_t)i, dtype);
+}
+
+void oracle_quantize_e4m3(int src_dtype, const void* src, int64_t n, float scale, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) {
+        float x = (float)orc_load(src, (size_t)i, src_dtype); /* exact: the source is <= 32 bits */
+        float y = x / scale;                                   /* binary32 division */
+        out[i] = oracle_e4m3_encode(y);
+    }
 }
 
 /* Physical slot of logical position `pos` of sequence `s`. */
@@ -116,8 +180,31 @@ int oracle_append(int dtype, int num_blocks, int block_size, int num_kv_heads, i
     return 0;
 }
 
+/* Append into an E4M3 pool: each K (V) row of src_dtype is quantized with
+ * k_scale (v_scale) and its codes written to the row's slot, as
+ * oracle_append does for plain rows. */
+int oracle_append_e4m3(int src_dtype, int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                       uint8_t* k_cache, uint8_t* v_cache, int n_tokens, const void* k, const void* v,
+                       const int32_t* slot_mapping, float k_scale, float v_scale) {
+    size_t srow = (size_t)head_dim * orc_elem_bytes(src_dtype);
+    for (int i = 0; i < n_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_blocks * block_size) return -1;
+        int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            size_t dst = (size_t)(((blk * num_kv_heads + h) * block_size + off)) * (size_t)head_dim;
+            size_t src = ((size_t)i * num_kv_heads + h) * srow;
+            oracle_quantize_e4m3(src_dtype, (const char*)k + src, head_dim, k_scale, k_cache + dst);
+            oracle_quantize_e4m3(src_dtype, (const char*)v + src, head_dim, v_scale, v_cache + dst);
+        }
+    }
+    return 0;
+}
+
 typedef struct {
-    int dtype;
+    int q_dtype, kv_dtype;
+    double k_scale, v_scale; /* a stored K (V) element stands for k_scale (v_scale) times its value */
     const void *q, *k_cache, *v_cache;
     const int32_t *tables, *ctx;
     int max_blocks, num_seqs, hq, hkv, d, bs, num_blocks;
@@ -152,11 +239,11 @@ static void* orc_attend_rows(void* arg) {
             int64_t off = t % J->bs;
             size_t base = (size_t)(((blk * J->hkv + h) * J->bs + off)) * D;
             for (int d = 0; d < D; ++d) {
-                K[(size_t)t * D + d] = orc_load(J->k_cache, base + d, J->dtype);
-                V[(size_t)t * D + d] = orc_load(J->v_cache, base + d, J->dtype);
+                K[(size_t)t * D + d] = J->k_scale * orc_load(J->k_cache, base + d, J->kv_dtype);
+                V[(size_t)t * D + d] = J->v_scale * orc_load(J->v_cache, base + d, J->kv_dtype);
             }
         }
-        for (int d = 0; d < D; ++d) qd[d] = orc_load(J->q, (size_t)r * D + d, J->dtype);
+        for (int d = 0; d < D; ++d) qd[d] = orc_load(J->q, (size_t)r * D + d, J->q_dtype);
         /* 2. scores */
         double mx = -INFINITY;
         for (int t = 0; t < n; ++t) {
@@ -185,12 +272,14 @@ static void* orc_attend_rows(void* arg) {
 
 /* out[s][g][d] (fp64) = softmax_t(scale * q[s][g] . K_s[t]) . V_s[t] over the
  * context_lens[s] tokens of sequence s; zero rows where the context is empty.
- * q is [num_seqs][Hq][D] in `dtype`.  nthreads <= 0 uses every online core.
+ * q is [num_seqs][Hq][D] in q_dtype, the cache in kv_dtype; a cache element
+ * stands for k_scale (v_scale) times its stored value.  nthreads <= 0 uses every online core.
  * Returns 0, or -1 if a table entry lies outside [0, num_blocks). */
-int oracle_paged_decode(int dtype, const void* q, const void* k_cache, const void* v_cache,
-                        const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
-                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                        int block_size, int num_blocks, double scale, double* out, int nthreads) {
+int oracle_paged_decode_scaled(int q_dtype, int kv_dtype, double k_scale, double v_scale,
+                               const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, double scale, double* out, int nthreads) {
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return -2;
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;
@@ -199,7 +288,7 @@ int oracle_paged_decode(int dtype, const void* q, const void* k_cache, const voi
     orc_job* jobs = (orc_job*)calloc((size_t)nthreads, sizeof(orc_job));
     pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int i = 0; i < nthreads; ++i) {
-        orc_job j = {dtype, q, k_cache, v_cache, block_tables, context_lens, max_blocks,
+        orc_job j = {q_dtype, kv_dtype, k_scale, v_scale, q, k_cache, v_cache, block_tables, context_lens, max_blocks,
                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                      scale, out, rows * i / nthreads, rows * (i + 1) / nthreads, 0};
         jobs[i] = j;
@@ -214,6 +303,16 @@ int oracle_paged_decode(int dtype, const void* q, const void* k_cache, const voi
     free(jobs);
     free(th);
     return status;
+}
+
+/* The same with q and the cache in one dtype and no cache scaling. */
+int oracle_paged_decode(int dtype, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int num_blocks, double scale, double* out, int nthreads) {
+    return oracle_paged_decode_scaled(dtype, dtype, 1.0, 1.0, q, k_cache, v_cache, block_tables,
+                                      max_blocks, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                      head_dim, block_size, num_blocks, scale, out, nthreads);
 }
 
 int oracle_num_cores(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }

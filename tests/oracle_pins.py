@@ -19,6 +19,16 @@ What pins what:
                   one token gives that token's V, a two-token case by hand),
                   an overwhelming score (exercises the max subtraction),
                   physical-block relabelling, equal heads in a group.
+  e4m3         -- torch's float8_e4m3fn conversions: decode of all 256 codes,
+                  encode of every midpoint between neighbouring codes (ties to
+                  even) and of random values below the overflow threshold;
+                  round trip of every finite code; the format's landmarks
+                  (1.0, 448, 2^-6, 2^-9); saturation from 448 up (the
+                  satfinite reading; torch itself gives NaN there).
+  fp8 append   -- the quantizing scatter reads back as torch's cast of the
+                  fp32 quotient x / scale; untouched slots keep their codes.
+  fp8 attention-- equals the brute force over the dequantized cache
+                  (scale * value), with different K and V scales.
 """
 from __future__ import annotations
 
@@ -287,6 +297,93 @@ def check_relabel_and_heads(lib):
     assert np.array_equal(got[1], got[0]), "shared table"
 
 
+# --------------------------------------------------------------------- E4M3
+def _torch_e4m3_codes(x_f32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x_f32, np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def check_e4m3_decoder(lib):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_values(codes, "e4m3", lib=lib)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(got, ref, equal_nan=True), "E4M3 decoder"
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF]), "E4M3 NaN codes"
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[0x08] == 2.0**-6 and got[0x01] == 2.0**-9
+
+
+def check_e4m3_encoder(lib):
+    enc = lambda x: oracle.e4m3_encode(x, lib=lib)  # noqa: E731
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.decode_values(codes, "e4m3", lib=lib)
+    for c, v in zip(codes, vals):
+        assert enc(float(v)) == c, f"round trip of code {c:#x}"
+    # Midpoints between neighbouring non-negative codes: exact ties.
+    pos = np.sort(vals[vals >= 0])
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    assert np.array_equal((pos[:-1] + pos[1:]) / 2, mids.astype(np.float64)), "midpoints exact in fp32"
+    got = np.array([enc(float(m)) for m in mids], dtype=np.uint8)
+    assert np.array_equal(got, _torch_e4m3_codes(mids)), "ties to even"
+    got = np.array([enc(float(-m)) for m in mids], dtype=np.uint8)
+    assert np.array_equal(got, _torch_e4m3_codes(-mids)), "negative ties"
+    rng = np.random.default_rng(8)
+    x = np.concatenate([rng.uniform(-463.9, 463.9, 3000), rng.standard_normal(3000) * 2.0**-7,
+                        rng.standard_normal(1000)]).astype(np.float32)
+    got = np.array([enc(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, _torch_e4m3_codes(x)), "random values"
+    for v in (448.0, 463.99, 464.0, 1e6, float("inf")):
+        assert enc(v) == 0x7E and enc(-v) == 0xFE, f"saturation at {v}"
+    assert enc(float("nan")) == 0x7F
+    assert enc(-0.0) == 0x80 and enc(0.0) == 0x00
+
+
+def check_fp8_append(lib):
+    rng = np.random.default_rng(31)
+    bs, Hkv, D, NB, n = 4, 2, 8, 6, 5
+    sentinel = np.full((NB, Hkv, bs, D), 0x55, np.uint8)
+    kp = torch.from_numpy(sentinel.copy()).view(torch.float8_e4m3fn)
+    vp = torch.from_numpy(sentinel.copy()).view(torch.float8_e4m3fn)
+    kn = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    vn = torch.from_numpy(rng.standard_normal((n, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    slots = np.array([3, 22, -1, 9, 0], np.int32)
+    ks, vs = 1.0 / 48.0, 0.0125
+    K, V = oracle.append_e4m3(kp, vp, kn, vn, slots, ks, vs, lib=lib)
+    K, V = K.view(torch.uint8).numpy(), V.view(torch.uint8).numpy()
+    written = np.zeros((NB, bs), bool)
+    for i, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        b, o = sl // bs, sl % bs
+        kq = (kn[i].float() / torch.tensor(ks, dtype=torch.float32)).numpy()
+        vq = (vn[i].float() / torch.tensor(vs, dtype=torch.float32)).numpy()
+        assert np.array_equal(K[b, :, o, :], _torch_e4m3_codes(kq)), "K codes"
+        assert np.array_equal(V[b, :, o, :], _torch_e4m3_codes(vq)), "V codes"
+        written[b, o] = True
+    assert np.all(K.transpose(0, 2, 1, 3)[~written] == 0x55) and np.all(V.transpose(0, 2, 1, 3)[~written] == 0x55)
+
+
+def check_fp8_attention(lib):
+    rng = np.random.default_rng(34)
+    ctx, Hq, Hkv, D, bs = [5, 1, 19, 16], 8, 2, 16, 4
+    NB = sum((c + bs - 1) // bs for c in ctx) + 3
+    tables = _random_tables(rng, ctx, bs, NB)
+    kp = torch.from_numpy(rng.integers(0, 256, (NB, Hkv, bs, D), dtype=np.uint8))
+    vp = torch.from_numpy(rng.integers(0, 256, (NB, Hkv, bs, D), dtype=np.uint8))
+    kp[(kp & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    vp[(vp & 0x7F) == 0x7F] = 0x44
+    q = torch.from_numpy(rng.standard_normal((len(ctx), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    ks, vs, scale = 0.004, 0.07, 0.25
+    got = oracle.paged_decode(q, kp.view(torch.float8_e4m3fn), vp.view(torch.float8_e4m3fn), tables,
+                              np.array(ctx, np.int32), scale, lib=lib, k_scale=ks, v_scale=vs)
+    kf = ks * kp.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    vf = vs * vp.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    Kc = [np.concatenate([kf[tables[s, j]] for j in range((c + bs - 1) // bs)], axis=1)[:, :c] for s, c in enumerate(ctx)]
+    Vc = [np.concatenate([vf[tables[s, j]] for j in range((c + bs - 1) // bs)], axis=1)[:, :c] for s, c in enumerate(ctx)]
+    ref = dense_attention(q.to(torch.float64).numpy(), Kc, Vc, scale, Hq // Hkv)
+    assert np.max(np.abs(got - ref)) < 1e-12, "fp8 attention vs dequantized brute force"
+
+
 ALL_CHECKS = [check_f16_decoder, check_bf16_decoder, check_f32_decoder, check_worked_slots,
               check_append_roundtrip, check_bruteforce, check_closed_forms,
-              check_relabel_and_heads]
+              check_relabel_and_heads, check_e4m3_decoder, check_e4m3_encoder, check_fp8_append,
+              check_fp8_attention]

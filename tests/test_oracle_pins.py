@@ -27,13 +27,23 @@ MUTATIONS = [
     ("last_token_dropped", "for (int t = 0; t < n; ++t) {\n            double w",
      "for (int t = 0; t + 1 < n; ++t) {\n            double w"),
     ("keys_as_values", "o[d] += w * V[", "o[d] += w * K["),
-    ("q_row_of_kv_head", "qd[d] = orc_load(J->q, (size_t)r * D + d, J->dtype);",
-     "qd[d] = orc_load(J->q, ((size_t)s * J->hq + h) * D + d, J->dtype);"),
+    ("q_row_of_kv_head", "qd[d] = orc_load(J->q, (size_t)r * D + d, J->q_dtype);",
+     "qd[d] = orc_load(J->q, ((size_t)s * J->hq + h) * D + d, J->q_dtype);"),
     ("append_transposed_layout",
      "size_t dst = (size_t)(((blk * num_kv_heads + h) * block_size + off)) * row;",
      "size_t dst = (size_t)(((blk * block_size + off) * num_kv_heads + h)) * row;"),
     ("half_subnormal_exponent", "v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -25);"),
     ("bf16_shift", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    ("e4m3_bias", "v = ldexp((double)(8 + frac), expo - 10);", "v = ldexp((double)(8 + frac), expo - 11);"),
+    ("e4m3_subnormal", "v = ldexp((double)frac, -9);", "v = ldexp((double)frac, -10);"),
+    ("e4m3_ties_odd", "(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    ("e4m3_ties_away", "(err == best_err && (c & 1) == 0)", "(err == best_err)"),
+    ("e4m3_overflow_nan", "if (a >= 448.0) return sign | 0x7e;", "if (a >= 464.0) return sign | 0x7f;"),
+    ("e4m3_sign_dropped", "return sign | (uint8_t)best;", "return (uint8_t)best;"),
+    ("quantize_multiplies", "float y = x / scale;", "float y = x * scale;"),
+    ("append_v_with_k_scale", "head_dim, v_scale, v_cache + dst);", "head_dim, k_scale, v_cache + dst);"),
+    ("attention_k_with_v_scale", "K[(size_t)t * D + d] = J->k_scale *", "K[(size_t)t * D + d] = J->v_scale *"),
+    ("attention_v_unscaled", "V[(size_t)t * D + d] = J->v_scale *", "V[(size_t)t * D + d] = 1.0 *"),
 ]
 
 
