@@ -207,7 +207,8 @@ class Step:
         B = len(pl.context_lens)
         self.B = B
         self.pool = pkv.KVPool(s.num_layers, pl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim,
-                               s.torch_dtype, device=device)
+                               s.cache_torch_dtype, device=device)
+        self.scales = dict(k_scale=s.kv_scales[0], v_scale=s.kv_scales[1]) if s.fp8 else {}
         self.layers = [self.pool.layer(l) for l in range(s.num_layers)]
         for l, (kc, vc) in enumerate(self.layers):
             fill_pool_layer(s, l, kc, vc)
@@ -239,11 +240,11 @@ class Step:
                 pkv.paged_decode_append_attention(self.q[l], self.kn[l], self.vn[l], kc, vc, self.tables,
                                                   self.ctx, s.attn_scale, seq_ids=self.seq_ids,
                                                   out=self.out[l], slot_mapping=self.slots,
-                                                  workspace=self.ws, **self.opts)
+                                                  workspace=self.ws, **self.scales, **self.opts)
             else:
-                self.pool.append(l, self.kn[l], self.vn[l], self.slots, seq_ids=self.seq_ids)
+                self.pool.append(l, self.kn[l], self.vn[l], self.slots, seq_ids=self.seq_ids, **self.scales)
                 pkv.paged_decode_attention(self.q[l], kc, vc, self.tables, self.ctx, s.attn_scale,
-                                           out=self.out[l], workspace=self.ws, **self.opts)
+                                           out=self.out[l], workspace=self.ws, **self.scales, **self.opts)
             if events is not None:
                 events[l][1].record()
 
@@ -267,7 +268,7 @@ def bench_ours(args, world, rank, local):
     B = step.B
     bytes_layer = roofline.attention_bytes(pl.context_lens, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                                            spec.elem_bytes, spec.block_size, spec.elem_bytes,
-                                           int(pl.appends.sum()))
+                                           int(pl.appends.sum()), kv_elem_bytes=spec.cache_elem_bytes)
     kv_bytes_step = bytes_layer.kv * spec.num_layers
 
     # Warm-up (eager), then parity spot check of the last layer against nothing
@@ -330,6 +331,8 @@ def bench_ours(args, world, rank, local):
     achieved = launch_bytes / (timed_launch_ms * 1e-3) / 1e9
     kernel_name = "paged_decode_partial_kernel<MmaPolicy>" if step.kernel != "ffma" else \
         "paged_decode_partial_kernel<FfmaPolicy>"
+    if spec.fp8:
+        kernel_name = "paged_decode_partial_kernel<MmaFp8Policy>"
     if step.fused:
         kernel_name += "_with_fused_append"
     traffic = recorded_traffic(kernel_name, spec.name)
@@ -373,12 +376,16 @@ def bench_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "accumulate": "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.cache_dtype, "accumulate": "f32",
+        "q_dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V, random block placement)",
         "config": {"workload": f"{spec.name}: {spec.num_layers} layers x {B} seqs x "
                                f"{int(pl.context_lens.max())} ctx (appended token included), "
                                f"{spec.num_q_heads}q/{spec.num_kv_heads}kv heads, D{spec.head_dim}, "
-                               f"{spec.dtype}, block {spec.block_size}, {pl.num_blocks}-block pool",
+                               f"{spec.dtype}" + (f" q, {spec.cache_dtype} cache (scales "
+                                                  f"{spec.kv_scales[0]:.6g}, {spec.kv_scales[1]:.6g})"
+                                                  if spec.fp8 else "") +
+                               f", block {spec.block_size}, {pl.num_blocks}-block pool",
                    "num_layers": spec.num_layers, "num_seqs": B, "context_tokens": int(pl.context_lens.sum()),
                    "kv_bytes_per_step": kv_bytes_step, "kernel": step.kernel,
                    "timing": "CUDA-graph replay of the whole step, CUDA events on the replay stream",
@@ -423,6 +430,9 @@ def oracle_sample(spec, pl, layer_pools=None, device="cpu"):
     remap[used] = np.arange(len(used), dtype=np.int32)
     tabs = np.where(rows >= 0, remap[np.maximum(rows, 0)], -1).astype(np.int32)
     idx = torch.from_numpy(used.astype(np.int64)).to(kc.device)
+    if kc.element_size() == 1:  # E4M3: gather through byte views
+        return (kc.view(torch.uint8)[idx].cpu().view(kc.dtype), vc.view(torch.uint8)[idx].cpu().view(vc.dtype),
+                tabs)
     return kc[idx].cpu(), vc[idx].cpu(), tabs
 
 
@@ -440,7 +450,9 @@ def cpu_baseline(spec, pl, seconds, step=None):
         q, _, _ = step_layer_values(spec, B, 0, "cpu")
     cores = oracle.num_cores()
     b = roofline.attention_bytes(pl.context_lens, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
-                                 spec.elem_bytes, spec.block_size, spec.elem_bytes, 0)
+                                 spec.elem_bytes, spec.block_size, spec.elem_bytes, 0,
+                                 kv_elem_bytes=spec.cache_elem_bytes)
+    scales = dict(k_scale=spec.kv_scales[0], v_scale=spec.kv_scales[1]) if spec.fp8 else {}
     # One sequence at a time, until the time budget is used (at least one).
     t0 = time.perf_counter()
     done_bytes = 0
@@ -448,8 +460,8 @@ def cpu_baseline(spec, pl, seconds, step=None):
     while True:
         s = n % B
         oracle.paged_decode(q[s:s + 1], kc, vc, tabs[s:s + 1], pl.context_lens[s:s + 1], spec.attn_scale,
-                            nthreads=cores)
-        done_bytes += int(pl.context_lens[s]) * spec.num_kv_heads * spec.head_dim * 2 * spec.elem_bytes
+                            nthreads=cores, **scales)
+        done_bytes += int(pl.context_lens[s]) * spec.num_kv_heads * spec.head_dim * 2 * spec.cache_elem_bytes
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
@@ -473,11 +485,13 @@ def bench_reference(args, world, rank):
     q, _, _ = step_layer_values(spec, B, 0, "cpu")
     cores = oracle.num_cores()
 
+    scales = dict(k_scale=spec.kv_scales[0], v_scale=spec.kv_scales[1]) if spec.fp8 else {}
+
     def one(i):
         s = i % B
         oracle.paged_decode(q[s:s + 1], kc, vc, tabs[s:s + 1], pl.context_lens[s:s + 1], spec.attn_scale,
-                            nthreads=cores)
-        return int(pl.context_lens[s]) * spec.num_kv_heads * spec.head_dim * 2 * spec.elem_bytes
+                            nthreads=cores, **scales)
+        return int(pl.context_lens[s]) * spec.num_kv_heads * spec.head_dim * 2 * spec.cache_elem_bytes
 
     for i in range(args.warmup):
         one(i)

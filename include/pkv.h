@@ -58,7 +58,13 @@ extern "C" {
 #pragma GCC visibility push(default)
 #endif
 
-typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype_t;
+/* KV_FP8_E4M3: one-byte E4M3 codes (sign, 4-bit exponent with bias 7, 3-bit
+ * fraction, no infinities, S.1111.111 = NaN, largest finite 448), a storage
+ * type of KV pools only ("vLLM Architecture and Installation", Example 6:
+ * an FP8 KV cache takes one byte per value).  A code b of a layer's K (V)
+ * stands for k_scale (v_scale) * e4m3(b); the scales are fp32, one per layer
+ * for K and one for V, owned by the caller and passed to every call. */
+typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2, KV_FP8_E4M3 = 3 } kv_dtype_t;
 
 typedef enum {
     KV_OK = 0,
@@ -290,6 +296,49 @@ kv_status_t paged_decode_attention_static(const void* q, const void* k_cache, co
  * bit was set, KV_ERR_DEVICE_TIMEOUT if the timeout bit was set, else
  * KV_ERR_DEVICE_CHECK. */
 kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out);
+
+/* ------------------------------------------------------- FP8 (E4M3) cache */
+
+/* kv_append into a KV_FP8_E4M3 pool: k and v are [n_tokens][Hkv][D] rows in
+ * src_dtype (KV_F32, KV_F16 or KV_BF16); each value x is stored as the E4M3
+ * code nearest to the fp32 quotient x / k_scale (x / v_scale), ties to the
+ * even code, magnitudes from 448 up saturating to +-448.  Otherwise as
+ * kv_append.  k_scale and v_scale must be finite and > 0. */
+kv_status_t kv_append_fp8(kv_pool_t* pool, int layer, const int32_t* seq_ids, int n_tokens,
+                          const void* k, const void* v, kv_dtype_t src_dtype,
+                          const int32_t* slot_mapping, float k_scale, float v_scale, void* stream);
+
+/* paged_decode_attention over an E4M3 cache ("vLLM Architecture and
+ * Installation", Example 6): the same attention with K = k_scale * e4m3(k
+ * code) and V = v_scale * e4m3(v code).  q is [num_seqs][Hq][D] in q_dtype
+ * (KV_F16 or KV_BF16; it enters the tensor cores as f16, exact for |q| below
+ * 65504 and above 2^-14); out_dtype is KV_F32 or q_dtype.  head_dim 128,
+ * block_size a multiple of 16 up to 256.  Workspace and options as
+ * paged_decode_attention (kernel KV_KERNEL_AUTO or KV_KERNEL_MMA). */
+kv_status_t paged_decode_attention_fp8(const void* q, kv_dtype_t q_dtype, const void* k_cache,
+                                       const void* v_cache, float k_scale, float v_scale,
+                                       int num_blocks, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float scale, void* out,
+                                       kv_dtype_t out_dtype, void* workspace,
+                                       size_t workspace_bytes, const kv_decode_options_t* opts,
+                                       void* stream);
+
+/* paged_decode_append_attention over an E4M3 cache: k_new and v_new are in
+ * q_dtype and are quantized as kv_append_fp8 does before this step reads
+ * them; otherwise as paged_decode_attention_fp8. */
+kv_status_t paged_decode_append_attention_fp8(const void* q, const void* k_new, const void* v_new,
+                                              const int32_t* seq_ids, kv_dtype_t q_dtype,
+                                              void* k_cache, void* v_cache, float k_scale,
+                                              float v_scale, int num_blocks,
+                                              const int32_t* block_tables, int max_blocks_per_seq,
+                                              const int32_t* context_lens, int num_seqs,
+                                              int num_q_heads, int num_kv_heads, int head_dim,
+                                              int block_size, float scale, void* out,
+                                              kv_dtype_t out_dtype, int32_t* slot_mapping,
+                                              void* workspace, size_t workspace_bytes,
+                                              const kv_decode_options_t* opts, void* stream);
 
 /* ------------------------------------------------------ swap to host memory */
 

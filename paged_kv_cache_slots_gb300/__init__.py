@@ -22,10 +22,13 @@ __all__ = [
     "make_workspace", "paged_decode_append_attention",
 ]
 
-KV_F32, KV_F16, KV_BF16 = 0, 1, 2
-DTYPE_CODE = {torch.float32: KV_F32, torch.float16: KV_F16, torch.bfloat16: KV_BF16}
+KV_F32, KV_F16, KV_BF16, KV_FP8_E4M3 = 0, 1, 2, 3
+DTYPE_CODE = {torch.float32: KV_F32, torch.float16: KV_F16, torch.bfloat16: KV_BF16,
+              torch.float8_e4m3fn: KV_FP8_E4M3}
 CODE_DTYPE = {v: k for k, v in DTYPE_CODE.items()}
-DTYPE_NAMES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+DTYPE_NAMES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+               "e4m3": torch.float8_e4m3fn, "fp8": torch.float8_e4m3fn}
+FP8 = torch.float8_e4m3fn
 KERNELS = {"auto": 0, "ffma": 1, "mma": 2}
 FLAG_BAD_BLOCK_ID, FLAG_BAD_SLOT, FLAG_BAD_CONTEXT, FLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
@@ -91,6 +94,13 @@ def _declare(lib):
                                    ctypes.POINTER(I), ctypes.POINTER(I)]),
         "kv_allocator_slot": (I, [P, I64, I, ctypes.POINTER(ctypes.c_int32)]),
         "kv_allocator_free_queue": (I, [P, ctypes.POINTER(ctypes.c_int32), I, ctypes.POINTER(I)]),
+        "kv_append_fp8": (I, [P, I, P, I, P, P, I, P, ctypes.c_float, ctypes.c_float, P]),
+        "paged_decode_attention_fp8": (I, [P, I, P, P, ctypes.c_float, ctypes.c_float, I, P, I, P, I,
+                                           I, I, I, I, ctypes.c_float, P, I, P, SZ,
+                                           ctypes.POINTER(_DecodeOptions), P]),
+        "paged_decode_append_attention_fp8": (I, [P, P, P, P, I, P, P, ctypes.c_float, ctypes.c_float,
+                                                  I, P, I, P, I, I, I, I, I, ctypes.c_float, P, I, P,
+                                                  P, SZ, ctypes.POINTER(_DecodeOptions), P]),
         "kv_swap_bytes": (SZ, [P, I]),
         "kv_swap_out": (I, [P, P, I, P, SZ, P]),
         "kv_swap_in": (I, [P, P, I, P, SZ, P]),
@@ -239,9 +249,26 @@ class KVPool:
         self._swap_keep = ids
 
     def append(self, layer: int, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
-               seq_ids: torch.Tensor | None = None, stream=None):
-        """Write k, v ([n, Hkv, D]) into this layer at slot_mapping ([n] int32)."""
+               seq_ids: torch.Tensor | None = None, stream=None, k_scale=None, v_scale=None):
+        """Write k, v ([n, Hkv, D]) into this layer at slot_mapping ([n] int32).
+
+        An E4M3 pool quantizes on the way and needs this layer's k_scale and
+        v_scale; k and v are then f32, f16 or bf16."""
         n = slot_mapping.shape[0]
+        if self.dtype == FP8:
+            _need(k_scale is not None and v_scale is not None, "an E4M3 pool needs k_scale and v_scale")
+            _need(k.dtype == v.dtype and k.dtype in (torch.float32, torch.float16, torch.bfloat16),
+                  "k/v must be f32, f16 or bf16")
+            _need(tuple(k.shape) == (n, self.cfg.num_kv_heads, self.cfg.head_dim) and k.shape == v.shape,
+                  "k and v must be [n_tokens, num_kv_heads, head_dim]")
+            _need(k.is_contiguous() and v.is_contiguous() and slot_mapping.is_contiguous(), "contiguous inputs")
+            _need(slot_mapping.dtype == torch.int32, "slot_mapping must be int32")
+            _need(seq_ids is None or (seq_ids.dtype == torch.int32 and seq_ids.shape[0] == n),
+                  "seq_ids must be int32 [n_tokens]")
+            _check(self._lib.kv_append_fp8(self._handle, layer, _ptr(seq_ids), n, _ptr(k), _ptr(v),
+                                           DTYPE_CODE[k.dtype], _ptr(slot_mapping), float(k_scale),
+                                           float(v_scale), _stream(k, stream)), self._lib)
+            return
         _need(k.dtype == self.dtype and v.dtype == self.dtype, "k/v dtype must match the pool")
         _need(tuple(k.shape) == (n, self.cfg.num_kv_heads, self.cfg.head_dim) and k.shape == v.shape,
               "k and v must be [n_tokens, num_kv_heads, head_dim]")
@@ -310,17 +337,24 @@ def workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, device=None, 
 
 
 def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                           out=None, out_dtype=None, workspace=None, stream=None, **opts):
+                           out=None, out_dtype=None, workspace=None, stream=None, k_scale=None,
+                           v_scale=None, **opts):
     """out[s, g] = softmax(scale q[s, g] . K_s^T) V_s over the paged cache (one layer).
 
     q [B, Hq, D]; k_cache/v_cache [NB, Hkv, bs, D]; block_tables int32 [B, max_blocks];
     context_lens int32 [B].  opts: num_ctas, ctas_per_sm, consumer_warps, kernel.
+    E4M3 (torch.float8_e4m3fn) caches stand for k_scale (v_scale) times their codes.
     """
     lib = load_library()
     B, Hq, D = q.shape
     NB, Hkv, bs, D2 = k_cache.shape
     _need(D == D2 and tuple(v_cache.shape) == tuple(k_cache.shape), "cache shapes")
-    _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and the caches share a dtype")
+    fp8 = k_cache.dtype == FP8
+    if fp8:
+        _need(v_cache.dtype == FP8 and k_scale is not None and v_scale is not None,
+              "an E4M3 cache needs both caches E4M3 and k_scale, v_scale")
+    else:
+        _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and the caches share a dtype")
     _need(all(t.is_contiguous() for t in (q, k_cache, v_cache, block_tables, context_lens)),
           "contiguous inputs")
     _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32, "int32 tables")
@@ -332,6 +366,13 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     o = _options(**opts)
     if workspace is None:
         workspace = make_workspace(B, Hq, Hkv, D, q.device, **opts)
+    if fp8:
+        _check(lib.paged_decode_attention_fp8(
+            _ptr(q), DTYPE_CODE[q.dtype], _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale),
+            NB, _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
+            float(scale), _ptr(out), DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(),
+            ctypes.byref(o), _stream(q, stream)), lib)
+        return out
     _check(lib.paged_decode_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), B, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale), _ptr(out),
@@ -342,7 +383,8 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
 
 def paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
                                   scale: float, seq_ids=None, out=None, out_dtype=None,
-                                  slot_mapping=None, workspace=None, stream=None, **opts):
+                                  slot_mapping=None, workspace=None, stream=None, k_scale=None,
+                                  v_scale=None, **opts):
     """One layer of a decode step in one kernel: append k_new/v_new ([B, Hkv, D]) at
     position context_lens - 1 of every sequence, then attend (see paged_decode_attention).
 
@@ -353,7 +395,13 @@ def paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, block_table
     B, Hq, D = q.shape
     NB, Hkv, bs, D2 = k_cache.shape
     _need(D == D2 and tuple(v_cache.shape) == tuple(k_cache.shape), "cache shapes")
-    _need(q.dtype == k_cache.dtype == v_cache.dtype == k_new.dtype == v_new.dtype, "one dtype")
+    fp8 = k_cache.dtype == FP8
+    if fp8:
+        _need(v_cache.dtype == FP8 and k_scale is not None and v_scale is not None,
+              "an E4M3 cache needs both caches E4M3 and k_scale, v_scale")
+        _need(q.dtype == k_new.dtype == v_new.dtype, "q, k_new and v_new share a dtype")
+    else:
+        _need(q.dtype == k_cache.dtype == v_cache.dtype == k_new.dtype == v_new.dtype, "one dtype")
     _need(tuple(k_new.shape) == (B, Hkv, D) and k_new.shape == v_new.shape, "k_new/v_new [B, Hkv, D]")
     _need(all(t.is_contiguous() for t in (q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)),
           "contiguous inputs")
@@ -369,6 +417,14 @@ def paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, block_table
     o = _options(**opts)
     if workspace is None:
         workspace = make_workspace(B, Hq, Hkv, D, q.device, **opts)
+    if fp8:
+        _check(lib.paged_decode_append_attention_fp8(
+            _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_ids), DTYPE_CODE[q.dtype], _ptr(k_cache),
+            _ptr(v_cache), float(k_scale), float(v_scale), NB, _ptr(block_tables), block_tables.shape[1],
+            _ptr(context_lens), B, Hq, Hkv, D, bs, float(scale), _ptr(out), DTYPE_CODE[out_dtype],
+            _ptr(slot_mapping), _ptr(workspace), workspace.numel(), ctypes.byref(o),
+            _stream(q, stream)), lib)
+        return out
     _check(lib.paged_decode_append_attention(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_ids), _ptr(k_cache), _ptr(v_cache), NB,
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,

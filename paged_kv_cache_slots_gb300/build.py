@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIBRARY = os.path.join(LIB_DIR, "libpkv.so")
-SOURCES = ["append.cu", "decode_plan.cu", "decode_ffma.cu", "decode_mma.cu", "decode_static.cu",
+SOURCES = ["append.cu", "decode_plan.cu", "decode_ffma.cu", "decode_mma.cu", "decode_fp8.cu",
+           "decode_static.cu",
            "prefix_pool.cpp", "swap.cu",
            "pkv_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

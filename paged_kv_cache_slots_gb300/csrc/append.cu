@@ -3,7 +3,9 @@
 // Follows "vLLM Architecture and Installation", Example 3 (paged KV cache
 // block tables): the slot of logical position p of a sequence is
 // table[p / block_size] * block_size + p % block_size, and each scheduled
-// token's new K and V rows are written to its slot.
+// token's new K and V rows are written to its slot.  Into an E4M3 pool (the
+// FP8 KV cache of Example 6 on the same page) each value is quantized on the
+// way: the code nearest to x / scale.
 #include "device_utils.cuh"
 
 namespace pkv {
@@ -28,6 +30,22 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
     }
     const int64_t blk = slot / a.block_size;
     const int64_t off = slot - blk * a.block_size;
+    if (a.quant) {
+        // E4M3 pool: lane e quantizes 16 elements of the K row (e < n) or of
+        // the V row (n <= e < 2n), n = head_dim / 16 output chunks.
+        const int n = a.head_dim >> 4;
+        const int64_t srow = static_cast<int64_t>(a.head_dim) * dtype_bytes(a.src_dtype);
+        const int64_t src = (static_cast<int64_t>(i) * a.num_kv_heads + h) * srow;
+        const int64_t dst = ((blk * a.num_kv_heads + h) * a.block_size + off) * a.head_dim;
+        for (int e = lane; e < 2 * n; e += 32) {
+            const bool isv = e >= n;
+            const int q = isv ? e - n : e;
+            const uint4 val = quantize_chunk16(static_cast<const char*>(isv ? a.v : a.k) + src, q,
+                                               a.src_dtype, isv ? a.v_scale : a.k_scale);
+            *reinterpret_cast<uint4*>(static_cast<char*>(isv ? a.v_cache : a.k_cache) + dst + 16 * q) = val;
+        }
+        return;
+    }
     const int64_t row_bytes = static_cast<int64_t>(a.head_dim) * a.elem_bytes;
     const int nvec = static_cast<int>(row_bytes >> 4);
     const int64_t src = (static_cast<int64_t>(i) * a.num_kv_heads + h) * row_bytes;

@@ -1,0 +1,272 @@
+// Tensor-core consumer of the split-context decode kernel for an E4M3 (FP8)
+// KV cache ("vLLM Architecture and Installation", Example 6: one byte per
+// cached value, so a block and the bytes a decode step reads halve).
+//
+// A cached byte b stands for scale * e4m3(b), one scale per layer for K and
+// one for V.  Every E4M3 value is exactly an f16, so the tile is converted in
+// registers (two codes per conversion) and fed to the f16 m16n8k16 MMA:
+//   S^T = K8 . Q^T           scores, times scale * log2(e) * k_scale
+//   O^T += V8^T . P^T        times v_scale when the state is written out
+// q (f16 or bf16) becomes f16 B fragments once per (sequence, head).
+//
+// Fragment layout.  ldmatrix moves 16-bit elements, i.e. pairs of codes.
+//  - K (non-transposed): a lane receives four consecutive codes of its row,
+//    dims 16j + 4c .. 16j + 4c + 3 of a 16-dim chunk j (c = lane % 4).  The
+//    dot product does not care in which order dims are summed, so the MMA's
+//    k index is permuted inside each chunk: logical columns 2c, 2c+1 hold
+//    dims 4c, 4c+1 and logical columns 2c+8, 2c+9 hold dims 4c+2, 4c+3, and
+//    the q fragments are built with the same permutation.  One ldmatrix.x4
+//    then yields the A fragments of two 16-dim chunks.
+//  - V (transposed): a lane receives the code pairs (2g, 2g+1) of tokens 2c
+//    and 2c+1 (g = lane / 4); a byte permute regroups them into the token
+//    pairs of dim 2g and of dim 2g+1.  So M row g of a 16-dim chunk is dim
+//    2g and row g+8 is dim 2g+1, and the output accumulators are written
+//    back with that mapping.
+// Tiles arrive through 2-D tensor maps with a 128-byte swizzle: rows of 128
+// codes (head_dim 128), chunk c of row r stored at chunk c ^ (r % 8).
+#include "decode_kernel.cuh"
+#include "mma_frag.cuh"
+
+namespace pkv {
+
+template <int QT, int D>
+struct MmaFp8Policy {
+    static_assert(D == 128, "E4M3 rows of 128 codes: one 128-byte slice per row");
+    static constexpr bool kTensor = true;
+    static constexpr bool kScratch = false;
+    static constexpr int KS = D / 16;  // 16-dim chunks: k-slices of QK, m-slices of PV
+    static constexpr int kD = D;
+    using T = typename Elem<QT>::T;
+
+    struct State {
+        uint32_t qb[KS][2];  // f16 B fragments of Q^T, head lane/4: dims 16ks + 4(lane%4) + {0,1} / {2,3}
+        float o[KS][4];      // O^T: dims 16mi + 2(lane/4) (+1 for [2],[3]), heads 2(lane%4) (+1 for [1],[3])
+        float m[2];          // running max of heads 2(lane%4), 2(lane%4)+1
+        float l[2];          // this lane's share of the running sum
+    };
+
+    __device__ __forceinline__ void begin(State& st, const DecodeArgs& a, int s, int h, int G) {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        const T* q = static_cast<const T*>(a.q) +
+                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            if (g < G) {
+                const uint2 raw = *reinterpret_cast<const uint2*>(q + 16 * ks + 4 * c);
+                if constexpr (QT == kF16) {
+                    st.qb[ks][0] = raw.x;
+                    st.qb[ks][1] = raw.y;
+                } else {
+                    const T* e = reinterpret_cast<const T*>(&raw);
+                    const __half2 h0 = __floats2half2_rn(Elem<QT>::to_float(e[0]), Elem<QT>::to_float(e[1]));
+                    const __half2 h1 = __floats2half2_rn(Elem<QT>::to_float(e[2]), Elem<QT>::to_float(e[3]));
+                    st.qb[ks][0] = *reinterpret_cast<const uint32_t*>(&h0);
+                    st.qb[ks][1] = *reinterpret_cast<const uint32_t*>(&h1);
+                }
+            } else {
+                st.qb[ks][0] = 0u;
+                st.qb[ks][1] = 0u;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) st.o[ks][r] = 0.f;
+        }
+        st.m[0] = st.m[1] = -INFINITY;
+        st.l[0] = st.l[1] = 0.f;
+    }
+
+    // One head's part of a stage: kt/vt point at the stage's K/V codes,
+    // [Hc*bs rows][128 B]; this warp's head owns rows hw*bs .. hw*bs+bs-1.
+    __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, uint8_t* kt, uint8_t* vt,
+                                         int hw, int n_valid, int, float*) {
+        const int lane = threadIdx.x & 31;
+        const int bs = a.block_size;
+        uint8_t* kh = kt + hw * bs * 128;
+        uint8_t* vh = vt + hw * bs * 128;
+        // Rows past the valid tokens may hold any code (even NaN): zero this
+        // head's V rows there so that 0 * V stays 0 in the PV product.
+        if (n_valid < bs) {
+            for (int e = lane; e < (bs - n_valid) * 8; e += 32) {
+                uint4* p = reinterpret_cast<uint4*>(vh + (n_valid + (e >> 3)) * 128 + ((e & 7) << 4));
+                *p = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+        const uint32_t kb = smem_addr(kh), vb = smem_addr(vh);
+        const uint32_t sw = lane & 7;  // swizzle key of the rows this lane addresses
+        const float sl = a.scale_log2;
+        // Lanes 0-7 / 8-15 / 16-23 / 24-31 address rows 0-7 / 8-15 / 0-7 / 8-15
+        // of the 16-token slice, in chunk 2p / 2p / 2p+1 / 2p+1.
+        const uint32_t rsel = static_cast<uint32_t>((lane & 7) + (lane & 8));
+        const uint32_t csel = static_cast<uint32_t>(lane >> 4);
+        for (int mt = 0; mt < bs / 16; ++mt) {
+            const uint32_t row = static_cast<uint32_t>(mt * 16) + rsel;
+            // ---- S^T = K . Q^T for tokens 16mt .. 16mt+15
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp) {
+                uint32_t r[4];
+                ldsm_x4(r, kb + row * 128u + ((((2u * kp) | csel) ^ sw) << 4));
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {  // chunk 2kp + hf: rows g / g+8 in r[2hf] / r[2hf+1]
+                    uint32_t af[4];
+                    af[0] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf]));
+                    af[1] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1]));
+                    af[2] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf] >> 16));
+                    af[3] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1] >> 16));
+                    mma16816<kF16>(acc, af, st.qb[2 * kp + hf][0], st.qb[2 * kp + hf][1]);
+                }
+            }
+            // ---- online softmax (heads 2c, 2c+1; tokens g and g+8 of the slice)
+            const int t0 = mt * 16 + (lane >> 2);
+            const bool v0 = t0 < n_valid, v1 = t0 + 8 < n_valid;
+            const float x0 = v0 ? acc[0] * sl : -INFINITY;
+            const float x1 = v0 ? acc[1] * sl : -INFINITY;
+            const float x2 = v1 ? acc[2] * sl : -INFINITY;
+            const float x3 = v1 ? acc[3] * sl : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+            const float al0 = fast_exp2(st.m[0] - mn0), al1 = fast_exp2(st.m[1] - mn1);
+            st.m[0] = mn0;
+            st.m[1] = mn1;
+            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+            st.l[0] = st.l[0] * al0 + (p0 + p2);
+            st.l[1] = st.l[1] * al1 + (p1 + p3);
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int mi = 0; mi < KS; ++mi) {
+                    st.o[mi][0] *= al0;
+                    st.o[mi][1] *= al1;
+                    st.o[mi][2] *= al0;
+                    st.o[mi][3] *= al1;
+                }
+            }
+            // ---- P^T fragments (k = token, n = head), f16 high + low parts
+            uint32_t h01, l01, h23, l23;
+            pack_split<kF16>(p0, p1, h01, l01);
+            pack_split<kF16>(p2, p3, h23, l23);
+            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+            const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+            // ---- O^T += V^T . P^T
+#pragma unroll
+            for (int mp = 0; mp < KS / 2; ++mp) {
+                uint32_t r[4];
+                ldsm_x4_trans(r, vb + row * 128u + ((((2u * mp) | csel) ^ sw) << 4));
+                // r[k] bytes: (tok 2c, dim 2g), (tok 2c, dim 2g+1), (tok 2c+1, dim 2g), (tok 2c+1, dim 2g+1);
+                // r[2hf] holds tokens 0-7 and r[2hf+1] tokens 8-15 of chunk 2mp + hf.
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const uint32_t lo = __byte_perm(r[2 * hf], 0u, 0x3120u);
+                    const uint32_t hi = __byte_perm(r[2 * hf + 1], 0u, 0x3120u);
+                    uint32_t af[4];
+                    af[0] = e4m3x2_to_half2(static_cast<uint16_t>(lo));        // dim 2g,   tokens 2c, 2c+1
+                    af[1] = e4m3x2_to_half2(static_cast<uint16_t>(lo >> 16));  // dim 2g+1, tokens 2c, 2c+1
+                    af[2] = e4m3x2_to_half2(static_cast<uint16_t>(hi));        // dim 2g,   tokens 8+2c, 9+2c
+                    af[3] = e4m3x2_to_half2(static_cast<uint16_t>(hi >> 16));  // dim 2g+1, tokens 8+2c, 9+2c
+                    mma16816<kF16>(st.o[2 * mp + hf], af, bh0, bh1);
+                    mma16816<kF16>(st.o[2 * mp + hf], af, bl0, bl1);
+                }
+            }
+        }
+        if (n_valid < bs) fence_proxy_async_smem();  // generic writes before the next TMA fill
+    }
+
+    // 16-byte chunk q of row r of head hw's tile (chunk c of a row lands at c ^ (row % 8)).
+    __device__ __forceinline__ void patch_chunk(const DecodeArgs& a, uint8_t* t, int hw, int r, int q,
+                                                uint4 val) const {
+        const int row = hw * a.block_size + r;
+        *reinterpret_cast<uint4*>(t + row * 128 + (((q & 7) ^ (row & 7)) << 4)) = val;
+    }
+
+    __device__ __forceinline__ void row_sums(const State& st, float& l0, float& l1) const {
+        l0 = st.l[0];
+        l1 = st.l[1];
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+    }
+
+    // v_scale * O (unnormalised) to o[g*os + d], (max, sum) to ml[g*ms], ml[g*ms + 1].
+    __device__ __forceinline__ void emit(const State& st, float vs, float* o, int os, float* ml, int ms,
+                                         int G) const {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        float l0, l1;
+        row_sums(st, l0, l1);
+        const int h0 = 2 * c, h1 = 2 * c + 1;
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+            const int d0 = 16 * mi + 2 * g;
+            if (h0 < G) {
+                o[h0 * os + d0] = st.o[mi][0] * vs;
+                o[h0 * os + d0 + 1] = st.o[mi][2] * vs;
+            }
+            if (h1 < G) {
+                o[h1 * os + d0] = st.o[mi][1] * vs;
+                o[h1 * os + d0 + 1] = st.o[mi][3] * vs;
+            }
+        }
+        if (g == 0) {
+            if (h0 < G) {
+                ml[h0 * ms] = st.m[0];
+                ml[h0 * ms + 1] = l0;
+            }
+            if (h1 < G) {
+                ml[h1 * ms] = st.m[1];
+                ml[h1 * ms + 1] = l1;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void write_state(const State& st, const DecodeArgs& a, float* dst,
+                                                int stride, int G) const {
+        emit(st, a.v_scale, dst, stride, dst + D, stride, G);
+    }
+
+    __device__ __forceinline__ void write_partial(const State& st, const DecodeArgs& a, float* o,
+                                                  float* ml, int G) const {
+        emit(st, a.v_scale, o, D, ml, 2, G);
+    }
+
+    // out[s][h*G + head][d] = v_scale * O / l in the output type.
+    __device__ __forceinline__ void write_final(const State& st, const DecodeArgs& a, int s, int h,
+                                                int G) const {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        float l0, l1;
+        row_sums(st, l0, l1);
+        const float i0 = a.v_scale / l0, i1 = a.v_scale / l1;
+        const int h0 = 2 * c, h1 = 2 * c + 1;
+        const int64_t base = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+            const int d0 = 16 * mi + 2 * g;
+            if (h0 < G) {
+                store_out(a.out, base + h0 * D + d0, st.o[mi][0] * i0, a.out_dtype);
+                store_out(a.out, base + h0 * D + d0 + 1, st.o[mi][2] * i0, a.out_dtype);
+            }
+            if (h1 < G) {
+                store_out(a.out, base + h1 * D + d0, st.o[mi][1] * i1, a.out_dtype);
+                store_out(a.out, base + h1 * D + d0 + 1, st.o[mi][3] * i1, a.out_dtype);
+            }
+        }
+    }
+};
+
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              cudaStream_t stream) {
+    if (a.kv_dtype != kFP8 || a.head_dim != 128) return cudaErrorInvalidValue;
+    if (a.dtype == kF16) return launch_partial<MmaFp8Policy<kF16, 128>>(a, tmk, tmv, stream);
+    if (a.dtype == kBF16) return launch_partial<MmaFp8Policy<kBF16, 128>>(a, tmk, tmv, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

@@ -142,7 +142,7 @@ static __device__ void build_prefix(const DecodeArgs& a, int chunks, int32_t* cu
 
 // ------------------------------------------------------------------ producer
 // kTensor: stages arrive through 2-D tensor maps with a 128-byte swizzle (box
-// of 64 elements x Hc*bs rows, one box per 64-element slice of the row);
+// of 128 bytes x Hc*bs rows, one box per 128-byte slice of the row);
 // otherwise as two plain contiguous bulk copies.
 template <bool kTensor>
 static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* full, uint64_t* empty,
@@ -151,7 +151,7 @@ static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* ful
     const int lane = threadIdx.x & 31;
     const uint64_t policy = policy_evict_first();
     const int stage_bytes = 2 * half_bytes;
-    const int64_t row_bytes = static_cast<int64_t>(a.head_dim) * dtype_bytes(a.dtype);
+    const int64_t row_bytes = static_cast<int64_t>(a.head_dim) * dtype_bytes(a.kv_dtype);
     int issued = 0;  // items whose copies were issued (lane 0)
     int stage = 0, round = 0;
     bool ok = true;
@@ -186,12 +186,15 @@ static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* ful
                     uint8_t* vd = kd + half_bytes;
                     mbar_arrive_expect_tx(&full[stage], stage_bytes);
                     if constexpr (kTensor) {
-                        const int slices = a.head_dim / 64;
+                        // One box per 128-byte slice of the row (64 f16/bf16
+                        // or 128 E4M3 elements).
+                        const int per = 128 / static_cast<int>(dtype_bytes(a.kv_dtype));
+                        const int slices = a.head_dim / per;
                         const int slice_bytes = half_bytes / slices;
                         for (int sl = 0; sl < slices; ++sl) {
-                            tensor_load_2d(kd + sl * slice_bytes, tmk, sl * 64, static_cast<int>(rk),
+                            tensor_load_2d(kd + sl * slice_bytes, tmk, sl * per, static_cast<int>(rk),
                                            &full[stage], policy);
-                            tensor_load_2d(vd + sl * slice_bytes, tmv, sl * 64, static_cast<int>(rk),
+                            tensor_load_2d(vd + sl * slice_bytes, tmv, sl * per, static_cast<int>(rk),
                                            &full[stage], policy);
                         }
                     } else {
@@ -393,16 +396,19 @@ __device__ __forceinline__ bool append_row(const DecodeArgs& a, const Policy& po
     // The slot is reported whether or not this sequence appends (as kv_slot_mapping does).
     if (a.slot_out && h == 0 && lane == 0) a.slot_out[s] = blk * a.block_size + r;
     if (a.append_ids && a.append_ids[s] < 0) return false;
-    const int eb = dtype_bytes(a.dtype);
-    const int nchunk = a.head_dim * eb / 16;  // 16-byte chunks of one row
+    const int eb = dtype_bytes(a.dtype);      // k_new / v_new
+    const int ce = dtype_bytes(a.kv_dtype);   // cache
+    const int nchunk = a.head_dim * ce / 16;  // 16-byte chunks of one cached row
     const int64_t src = (static_cast<int64_t>(s) * a.num_kv_heads + h) * a.head_dim * eb;
     const int64_t dst = ((static_cast<int64_t>(blk) * a.num_kv_heads + h) * a.block_size + r) *
-                        static_cast<int64_t>(a.head_dim) * eb;
+                        static_cast<int64_t>(a.head_dim) * ce;
     for (int e = lane; e < 2 * nchunk; e += 32) {
         const bool isv = e >= nchunk;
         const int q = isv ? e - nchunk : e;
-        const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                              static_cast<const char*>(isv ? a.v_new : a.k_new) + src) + q);
+        const char* row = static_cast<const char*>(isv ? a.v_new : a.k_new) + src;
+        const uint4 val = a.kv_dtype == kFP8
+                              ? quantize_chunk16(row, q, a.dtype, isv ? a.v_scale : a.k_scale)
+                              : __ldg(reinterpret_cast<const uint4*>(row) + q);
         *(reinterpret_cast<uint4*>(const_cast<char*>(
               static_cast<const char*>(isv ? a.v_cache : a.k_cache)) + dst) + q) = val;
         pol.patch_chunk(a, isv ? vt : kt, hw, r, q, val);
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(32 * 16, 1)
     const int Hc = a.heads_per_stage, R = a.warps_per_head, NC = a.consumer_warps;
     const int chunks = a.num_kv_heads / Hc;
     const int D = a.head_dim;
-    const int half_bytes = Hc * a.block_size * D * dtype_bytes(a.dtype);
+    const int half_bytes = Hc * a.block_size * D * dtype_bytes(a.kv_dtype);
     const SmemLayout L = smem_layout(a.stages, half_bytes, a.num_seqs, NC, R, G, D, a.block_size,
                                      Policy::kScratch);
     uint8_t* ring = base + L.ring;

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include <utility>
@@ -177,6 +178,46 @@ struct Elem<kBF16> {
     static __device__ __forceinline__ float to_float(T x) { return __bfloat162float(x); }
     static __device__ __forceinline__ T from_float(float x) { return __float2bfloat16_rn(x); }
 };
+
+// ------------------------------------------------------------------- E4M3
+// A cached E4M3 byte b stands for scale * e4m3(b); a value x is stored as the
+// E4M3 code nearest to the fp32 quotient x / scale (round to nearest even,
+// saturating at +-448, the conversion instruction's satfinite mode).
+
+// Loads element i of a row of src_dtype (f32, f16 or bf16) as fp32.
+__device__ __forceinline__ float load_as_float(const void* row, int i, int src_dtype) {
+    if (src_dtype == kF32) return static_cast<const float*>(row)[i];
+    if (src_dtype == kF16) return __half2float(static_cast<const __half*>(row)[i]);
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(row)[i]);
+}
+
+// Two fp32 values -> two E4M3 codes (x0 in the low byte).
+__device__ __forceinline__ uint16_t e4m3x2_from_floats(float x0, float x1) {
+    return static_cast<uint16_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Codes of elements 16q .. 16q+15 of a source row (src_dtype), each divided
+// by `scale` in fp32 first: one 16-byte chunk of a quantized row.
+__device__ __forceinline__ uint4 quantize_chunk16(const void* row, int q, int src_dtype, float scale) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = 16 * q + 4 * k;
+        const uint16_t lo = e4m3x2_from_floats(__fdiv_rn(load_as_float(row, i, src_dtype), scale),
+                                               __fdiv_rn(load_as_float(row, i + 1, src_dtype), scale));
+        const uint16_t hi = e4m3x2_from_floats(__fdiv_rn(load_as_float(row, i + 2, src_dtype), scale),
+                                               __fdiv_rn(load_as_float(row, i + 3, src_dtype), scale));
+        w[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Two E4M3 codes (low byte first) -> f16x2 (exact: every E4M3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t v) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
 
 // Store an fp32 value as out_dtype (round to nearest even).
 __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int out_dtype) {

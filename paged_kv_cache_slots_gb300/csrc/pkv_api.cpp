@@ -38,6 +38,8 @@ kv_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 bool valid_dtype(int d) { return d == KV_F32 || d == KV_F16 || d == KV_BF16; }
+bool valid_pool_dtype(int d) { return valid_dtype(d) || d == KV_FP8_E4M3; }
+bool valid_scale(float x) { return std::isfinite(x) && x > 0.f; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -169,17 +171,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D view of one layer's cache: rows = num_blocks*Hkv*bs, row = head_dim
-// elements; box = 64 elements x box_rows rows (Hc heads of one block),
-// 128-byte swizzle.
+// elements; box = 128 bytes (64 f16/bf16 or 128 E4M3 elements) x box_rows
+// rows (Hc heads of one block), 128-byte swizzle.
 kv_status_t encode_cache_map(CUtensorMap* map, const void* base, int dtype, int rows, int head_dim,
                              int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int eb = dtype_bytes(dtype);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * eb};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(map, dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    const CUtensorMapDataType type = dtype == KV_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : dtype == KV_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = enc(map, type,
                      2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -298,7 +304,7 @@ const char* kv_last_error(void) { return g_last_error; }
 
 size_t kv_pool_bytes(const kv_pool_config_t* c) {
     if (!c || c->num_layers <= 0 || c->num_blocks <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 ||
-        c->head_dim <= 0 || !valid_dtype(c->dtype))
+        c->head_dim <= 0 || !valid_pool_dtype(c->dtype))
         return 0;
     return 2ull * c->num_layers * c->num_blocks * c->block_size * c->num_kv_heads * c->head_dim *
            static_cast<size_t>(dtype_bytes(c->dtype));
@@ -394,6 +400,8 @@ kv_status_t kv_append(kv_pool_t* p, int layer, const int32_t* seq_ids, int n_tok
                       const void* v, const int32_t* slot_mapping, void* stream) {
     if (!p) return fail(KV_ERR_INVALID_ARG, "kv_append: null pool");
     if (n_tokens < 0) return fail(KV_ERR_INVALID_ARG, "kv_append: n_tokens %d", n_tokens);
+    if (p->cfg.dtype == KV_FP8_E4M3)
+        return fail(KV_ERR_INVALID_ARG, "kv_append: an E4M3 pool takes kv_append_fp8 (with scales)");
     void *kc = nullptr, *vc = nullptr;
     if (kv_status_t st = kv_pool_layer(p, layer, &kc, &vc)) return st;
     if (n_tokens == 0) return KV_OK;
@@ -405,7 +413,38 @@ kv_status_t kv_append(kv_pool_t* p, int layer, const int32_t* seq_ids, int n_tok
     uint32_t* status = nullptr;
     if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
     AppendArgs a{seq_ids, k, v, slot_mapping, kc, vc, status, n_tokens, p->cfg.num_kv_heads,
-                 p->cfg.head_dim, p->cfg.block_size, p->cfg.num_blocks, dtype_bytes(p->cfg.dtype), 1};
+                 p->cfg.head_dim, p->cfg.block_size, p->cfg.num_blocks, dtype_bytes(p->cfg.dtype), 1,
+                 0, p->cfg.dtype, 1.f, 1.f};
+    cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return KV_OK;
+}
+
+kv_status_t kv_append_fp8(kv_pool_t* p, int layer, const int32_t* seq_ids, int n_tokens, const void* k,
+                          const void* v, kv_dtype_t src_dtype, const int32_t* slot_mapping, float k_scale,
+                          float v_scale, void* stream) {
+    if (!p) return fail(KV_ERR_INVALID_ARG, "kv_append_fp8: null pool");
+    if (p->cfg.dtype != KV_FP8_E4M3)
+        return fail(KV_ERR_INVALID_ARG, "kv_append_fp8: the pool is not KV_FP8_E4M3");
+    if (!valid_dtype(src_dtype)) return fail(KV_ERR_INVALID_ARG, "kv_append_fp8: source dtype %d", src_dtype);
+    if (!valid_scale(k_scale) || !valid_scale(v_scale))
+        return fail(KV_ERR_INVALID_ARG, "kv_append_fp8: scales must be finite and > 0");
+    if (n_tokens < 0) return fail(KV_ERR_INVALID_ARG, "kv_append_fp8: n_tokens %d", n_tokens);
+    if (p->cfg.head_dim % 16)
+        return fail(KV_ERR_UNSUPPORTED, "kv_append_fp8: head_dim must be a multiple of 16");
+    void *kc = nullptr, *vc = nullptr;
+    if (kv_status_t st = kv_pool_layer(p, layer, &kc, &vc)) return st;
+    if (n_tokens == 0) return KV_OK;
+    if (!k || !v || !slot_mapping) return fail(KV_ERR_INVALID_ARG, "kv_append_fp8: null pointer");
+    if (!aligned(k, 16) || !aligned(v, 16))
+        return fail(KV_ERR_INVALID_ARG, "kv_append_fp8: k and v must be 16-byte aligned");
+    if (static_cast<int64_t>(n_tokens) * p->cfg.num_kv_heads >= (int64_t{1} << 31) / 32)
+        return fail(KV_ERR_UNSUPPORTED, "kv_append_fp8: too many tokens in one call");
+    uint32_t* status = nullptr;
+    if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
+    AppendArgs a{seq_ids, k, v, slot_mapping, kc, vc, status, n_tokens, p->cfg.num_kv_heads,
+                 p->cfg.head_dim, p->cfg.block_size, p->cfg.num_blocks, 1, 1,
+                 1, src_dtype, k_scale, v_scale};
     cudaError_t e = launch_append(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return KV_OK;
@@ -462,7 +501,9 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
                                int block_size, kv_dtype_t dtype, float scale, void* out,
                                kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
                                const kv_decode_options_t* opts, void* stream, const void* k_new,
-                               const void* v_new, const int32_t* append_ids, int32_t* slot_out) {
+                               const void* v_new, const int32_t* append_ids, int32_t* slot_out,
+                               kv_dtype_t kv_dtype, float k_scale, float v_scale) {
+    const bool fp8 = kv_dtype == KV_FP8_E4M3;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
         return fail(KV_ERR_INVALID_ARG, "paged_decode_attention: sizes out of range");
     if (num_q_heads % num_kv_heads)
@@ -475,6 +516,15 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     if (block_size < 1 || block_size > 256) return fail(KV_ERR_UNSUPPORTED, "block_size %d", block_size);
     if (!valid_dtype(dtype) || !valid_dtype(out_dtype))
         return fail(KV_ERR_INVALID_ARG, "unknown dtype");
+    if (fp8) {
+        if (dtype != KV_F16 && dtype != KV_BF16)
+            return fail(KV_ERR_UNSUPPORTED, "an E4M3 cache takes an f16 or bf16 q");
+        if (head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "an E4M3 cache needs head_dim 128");
+        if (!valid_scale(k_scale) || !valid_scale(v_scale))
+            return fail(KV_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
+    } else if (kv_dtype != dtype) {
+        return fail(KV_ERR_INVALID_ARG, "the cache must have q's dtype (or be E4M3)");
+    }
     if (out_dtype != KV_F32 && out_dtype != dtype)
         return fail(KV_ERR_UNSUPPORTED, "out_dtype must be KV_F32 or the input dtype");
     if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale is not finite");
@@ -488,6 +538,9 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     if (kernel == KV_KERNEL_AUTO) kernel = mma_ok ? KV_KERNEL_MMA : KV_KERNEL_FFMA;
     if (kernel == KV_KERNEL_MMA && !mma_ok)
         return fail(KV_ERR_UNSUPPORTED, "tensor-core kernel needs f16/bf16 and block_size % 16 == 0");
+    if (fp8 && kernel != KV_KERNEL_MMA)
+        return fail(KV_ERR_UNSUPPORTED, "an E4M3 cache is read by the tensor-core kernel only "
+                                        "(block_size a multiple of 16)");
     if (num_seqs == 0) return KV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
         return fail(KV_ERR_INVALID_ARG, "paged_decode_attention: null pointer");
@@ -510,7 +563,7 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     // Head chunking and warps: Hc KV heads per stage, R warps per head.
     int hc = o.heads_per_stage;
     if (hc == 0) {
-        hc = auto_heads_per_stage(num_kv_heads, block_size, head_dim, dtype, kernel == KV_KERNEL_MMA);
+        hc = auto_heads_per_stage(num_kv_heads, block_size, head_dim, kv_dtype, kernel == KV_KERNEL_MMA);
     } else if (num_kv_heads % hc) {
         return fail(KV_ERR_INVALID_ARG, "heads_per_stage %d does not divide num_kv_heads %d", hc,
                     num_kv_heads);
@@ -532,7 +585,7 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     DecodePlan plan{};
     bool planned = false;
     for (; R >= 1; --R) {
-        planned = decode_plan(kernel, dtype, head_dim, block_size, G, num_seqs, hc, R, budget, &plan);
+        planned = decode_plan(kernel, kv_dtype, head_dim, block_size, G, num_seqs, hc, R, budget, &plan);
         if (planned && (plan.stages >= 2 * R || R == 1)) break;
         if (planned && o.consumer_warps) break;  // an explicit warp count is kept if it fits at all
     }
@@ -560,7 +613,11 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     a.block_size = block_size;
     a.dtype = dtype;
     a.out_dtype = out_dtype;
-    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.kv_dtype = kv_dtype;
+    a.k_scale = fp8 ? k_scale : 1.f;
+    a.v_scale = fp8 ? v_scale : 1.f;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 *
+                                      static_cast<double>(a.k_scale));
     a.num_ctas = P;
     a.heads_per_stage = hc;
     a.warps_per_head = R;
@@ -582,9 +639,9 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     if (kernel == KV_KERNEL_MMA) {
         CUtensorMap tk, tv;
         const int rows = num_blocks * num_kv_heads * block_size;
-        if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, hc * block_size)) return st;
-        if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, hc * block_size)) return st;
-        e = launch_decode_mma(a, tk, tv, s);
+        if (kv_status_t st = encode_cache_map(&tk, k_cache, kv_dtype, rows, head_dim, hc * block_size)) return st;
+        if (kv_status_t st = encode_cache_map(&tv, v_cache, kv_dtype, rows, head_dim, hc * block_size)) return st;
+        e = fp8 ? launch_decode_fp8(a, tk, tv, s) : launch_decode_mma(a, tk, tv, s);
     } else {
         e = launch_decode_ffma(a, s);
     }
@@ -604,7 +661,8 @@ kv_status_t paged_decode_attention(const void* q, const void* k_cache, const voi
                                    const kv_decode_options_t* opts, void* stream) {
     return decode_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
                        num_q_heads, num_kv_heads, head_dim, block_size, dtype, scale, out, out_dtype,
-                       workspace, workspace_bytes, opts, stream, nullptr, nullptr, nullptr, nullptr);
+                       workspace, workspace_bytes, opts, stream, nullptr, nullptr, nullptr, nullptr,
+                       dtype, 1.f, 1.f);
 }
 
 kv_status_t paged_decode_append_attention(const void* q, const void* k_new, const void* v_new,
@@ -620,7 +678,39 @@ kv_status_t paged_decode_append_attention(const void* q, const void* k_new, cons
         return fail(KV_ERR_INVALID_ARG, "paged_decode_append_attention: null k_new / v_new");
     return decode_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
                        num_q_heads, num_kv_heads, head_dim, block_size, dtype, scale, out, out_dtype,
-                       workspace, workspace_bytes, opts, stream, k_new, v_new, seq_ids, slot_mapping);
+                       workspace, workspace_bytes, opts, stream, k_new, v_new, seq_ids, slot_mapping,
+                       dtype, 1.f, 1.f);
+}
+
+kv_status_t paged_decode_attention_fp8(const void* q, kv_dtype_t q_dtype, const void* k_cache,
+                                       const void* v_cache, float k_scale, float v_scale, int num_blocks,
+                                       const int32_t* block_tables, int max_blocks,
+                                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int block_size, float scale,
+                                       void* out, kv_dtype_t out_dtype, void* workspace,
+                                       size_t workspace_bytes, const kv_decode_options_t* opts,
+                                       void* stream) {
+    return decode_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, q_dtype, scale, out, out_dtype,
+                       workspace, workspace_bytes, opts, stream, nullptr, nullptr, nullptr, nullptr,
+                       KV_FP8_E4M3, k_scale, v_scale);
+}
+
+kv_status_t paged_decode_append_attention_fp8(const void* q, const void* k_new, const void* v_new,
+                                              const int32_t* seq_ids, kv_dtype_t q_dtype, void* k_cache,
+                                              void* v_cache, float k_scale, float v_scale, int num_blocks,
+                                              const int32_t* block_tables, int max_blocks,
+                                              const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                              int num_kv_heads, int head_dim, int block_size, float scale,
+                                              void* out, kv_dtype_t out_dtype, int32_t* slot_mapping,
+                                              void* workspace, size_t workspace_bytes,
+                                              const kv_decode_options_t* opts, void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return fail(KV_ERR_INVALID_ARG, "paged_decode_append_attention_fp8: null k_new / v_new");
+    return decode_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, q_dtype, scale, out, out_dtype,
+                       workspace, workspace_bytes, opts, stream, k_new, v_new, seq_ids, slot_mapping,
+                       KV_FP8_E4M3, k_scale, v_scale);
 }
 
 kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out) {

@@ -12,9 +12,9 @@
 namespace pkv {
 
 // Element types as stored in the pool, q and out (same codes as kv_dtype_t).
-enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2, kFP8 = 3 };
 
-__host__ __device__ inline int dtype_bytes(int dt) { return dt == kF32 ? 4 : 2; }
+__host__ __device__ inline int dtype_bytes(int dt) { return dt == kF32 ? 4 : dt == kFP8 ? 1 : 2; }
 
 struct AppendArgs {
     const int32_t* seq_ids;       // [n_tokens] or nullptr
@@ -26,6 +26,11 @@ struct AppendArgs {
     uint32_t* status;             // device status word
     int n_tokens, num_kv_heads, head_dim, block_size, num_blocks, elem_bytes;
     int pdl;
+    // Quantizing append into an E4M3 pool: k/v rows are in src_dtype and
+    // are stored as codes of x / k_scale (x / v_scale).
+    int quant;
+    int src_dtype;
+    float k_scale, v_scale;
 };
 
 // Block swap between the pool and a device-addressable host buffer.
@@ -76,8 +81,10 @@ struct DecodeArgs {
     const int32_t* append_ids;   // [num_seqs] or nullptr; a negative entry: no append for s
     int32_t* slot_out;           // [num_seqs] or nullptr: slot of the newest token
     int num_blocks, max_blocks, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
-    int dtype, out_dtype;
-    float scale_log2;     // scale * log2(e): scores are kept in base-2 units
+    int dtype, out_dtype;  // q (and k_new, v_new) and output types
+    int kv_dtype;          // cache type: dtype, or kFP8 (E4M3 codes)
+    float scale_log2;      // scale * log2(e) (* k_scale for E4M3): scores in base-2 units
+    float k_scale, v_scale;  // E4M3 cache: a code stands for scale * value (1 otherwise)
     int num_ctas;         // persistent grid size P
     int heads_per_stage;  // Hc: KV heads per pipeline stage (divides Hkv)
     int warps_per_head;   // R: consumer warps sharing one head's items
@@ -106,6 +113,8 @@ cudaError_t launch_slot_mapping(const SlotArgs& a, cudaStream_t stream);
 cudaError_t launch_swap(const SwapArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_ffma(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k,
                               const CUtensorMap& tmap_v, cudaStream_t stream);
 cudaError_t launch_decode_reduce(const DecodeArgs& a, cudaStream_t stream);
 

@@ -56,14 +56,19 @@ class AttentionBytes:
 
 def attention_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
                     elem_bytes: int, block_size: int, out_elem_bytes: int,
-                    appended_tokens: int) -> AttentionBytes:
-    """Algorithmic bytes of one layer: split partials and the reduce are overhead, not counted."""
+                    appended_tokens: int, kv_elem_bytes: int | None = None) -> AttentionBytes:
+    """Algorithmic bytes of one layer: split partials and the reduce are overhead, not counted.
+
+    elem_bytes: q and the new K/V rows; kv_elem_bytes: the cache (default
+    elem_bytes; 1 for an E4M3 cache, whose append reads elem_bytes per value
+    and writes one byte)."""
+    kvb = elem_bytes if kv_elem_bytes is None else kv_elem_bytes
     ctx = np.asarray(context_lens, dtype=np.int64)
     B = len(ctx)
-    kv = int(ctx.sum()) * num_kv_heads * head_dim * 2 * elem_bytes
+    kv = int(ctx.sum()) * num_kv_heads * head_dim * 2 * kvb
     q = B * num_q_heads * head_dim * elem_bytes
     out = B * num_q_heads * head_dim * out_elem_bytes
     tables = int(((ctx + block_size - 1) // block_size).sum()) * 4
     lens = B * 4
-    append = 2 * (2 * appended_tokens * num_kv_heads * head_dim * elem_bytes) + appended_tokens * 4
+    append = 2 * appended_tokens * num_kv_heads * head_dim * (elem_bytes + kvb) + appended_tokens * 4
     return AttentionBytes(kv, q, out, tables, lens, append)

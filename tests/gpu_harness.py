@@ -41,15 +41,19 @@ def check_output(out: torch.Tensor, ref: np.ndarray, what: str):
     return float(err.max()) if err.size else 0.0
 
 
+def _ws_opts(opts):
+    return {k: v for k, v in opts.items() if k not in ("test_stall", "k_scale", "v_scale")}
+
+
 def attend(q, kc, vc, tables, ctx, scale, out_dtype=None, **opts):
     """paged_decode_attention with a NaN-filled output and an 0xFF-filled
     workspace, so that an output the kernels fail to write, or a partial they
-    read without having written it, cannot pass unnoticed."""
+    read without having written it, cannot pass unnoticed.  An E4M3 cache
+    takes k_scale and v_scale in opts."""
     B, Hq, D = q.shape
     out_dtype = out_dtype or q.dtype
     out = torch.full((B, Hq, D), float("nan"), dtype=out_dtype, device=q.device)
-    n = pkv.workspace_bytes(B, Hq, kc.shape[1], D, q.device,
-                            **{k: v for k, v in opts.items() if k != "test_stall"})
+    n = pkv.workspace_bytes(B, Hq, kc.shape[1], D, q.device, **_ws_opts(opts))
     ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=q.device)
     pkv.workspace_init(ws, B, kc.shape[1])  # only the merge counters must start at zero
     return pkv.paged_decode_attention(q, kc, vc, tables, ctx, scale, out=out, out_dtype=out_dtype,
@@ -62,13 +66,40 @@ def attend_append(q, kn, vn, kc, vc, tables, ctx, scale, seq_ids=None, out_dtype
     out_dtype = out_dtype or q.dtype
     out = torch.full((B, Hq, D), float("nan"), dtype=out_dtype, device=q.device)
     slots = torch.full((B,), -7, dtype=torch.int32, device=q.device)
-    n = pkv.workspace_bytes(B, Hq, kc.shape[1], D, q.device,
-                            **{k: v for k, v in opts.items() if k != "test_stall"})
+    n = pkv.workspace_bytes(B, Hq, kc.shape[1], D, q.device, **_ws_opts(opts))
     ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=q.device)
     pkv.workspace_init(ws, B, kc.shape[1])
     pkv.paged_decode_append_attention(q, kn, vn, kc, vc, tables, ctx, scale, seq_ids=seq_ids, out=out,
                                       out_dtype=out_dtype, slot_mapping=slots, workspace=ws, **opts)
     return out, slots
+
+
+def scale_opts(spec) -> dict:
+    """k_scale / v_scale arguments of an E4M3 spec (none otherwise)."""
+    return dict(k_scale=spec.kv_scales[0], v_scale=spec.kv_scales[1]) if spec.fp8 else {}
+
+
+def oracle_append(spec, k_pre, v_pre, kn, vn, slots):
+    """The oracle's append for the spec's cache type."""
+    if spec.fp8:
+        return oracle.append_e4m3(k_pre, v_pre, kn, vn, slots, *spec.kv_scales)
+    return oracle.append(k_pre, v_pre, kn, vn, slots)
+
+
+def oracle_attention(spec, q, k, v, tables, ctx):
+    return oracle.paged_decode(q, k, v, tables, ctx, spec.attn_scale, **scale_opts(spec))
+
+
+def take(t: torch.Tensor, idx: torch.Tensor) -> torch.Tensor:
+    """t[idx] along dim 0 (through a byte view for one-byte types)."""
+    if t.element_size() == 1:
+        return t.view(torch.uint8)[idx].view(t.dtype)
+    return t[idx]
+
+
+def cache_bits(t: torch.Tensor) -> torch.Tensor:
+    """Bit patterns of a cache of any type (E4M3 as bytes)."""
+    return t.view(torch.uint8) if t.element_size() == 1 else bits(t)
 
 
 def newest_slot_masks(placement):
@@ -88,15 +119,15 @@ class SmallCase:
         """(slots, K after append, V after append, fp64 attention output)."""
         sl = oracle.slot_mapping(self.pl.block_tables, self.pl.context_lens, self.spec.block_size)
         sl_w = np.where(self.pl.appends, sl, -1).astype(np.int32)
-        kpost, vpost = oracle.append(self.kpool, self.vpool, self.kn, self.vn, sl_w)
-        ref = oracle.paged_decode(self.q, kpost, vpost, self.pl.block_tables, self.pl.context_lens,
-                                  self.spec.attn_scale)
+        kpost, vpost = oracle_append(self.spec, self.kpool, self.vpool, self.kn, self.vn, sl_w)
+        ref = oracle_attention(self.spec, self.q, kpost, vpost, self.pl.block_tables,
+                               self.pl.context_lens)
         return sl, kpost, vpost, ref
 
     def device(self, dev="cuda"):
         s = self.spec
         pool = pkv.KVPool(s.num_layers, self.pl.num_blocks, s.block_size, s.num_kv_heads,
-                          s.head_dim, s.torch_dtype, device=dev)
+                          s.head_dim, s.cache_torch_dtype, device=dev)
         kc, vc = pool.layer(self.layer)
         kc.copy_(self.kpool)
         vc.copy_(self.vpool)
@@ -111,9 +142,9 @@ class SmallCase:
 def run_step(d, spec, num_blocks, layer=0, out_dtype=None, **opts):
     """Slot mapping, append and attention of one layer through the library."""
     slots = pkv.slot_mapping(d["tables"], d["ctx"], spec.block_size, num_blocks)
-    d["pool"].append(layer, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
+    d["pool"].append(layer, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"], **scale_opts(spec))
     out = attend(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
-                 out_dtype=out_dtype, **opts)
+                 out_dtype=out_dtype, **scale_opts(spec), **opts)
     return slots, out
 
 
@@ -134,7 +165,7 @@ class LargeCase:
         self.spec, self.pl, self.dev = spec, placement, dev
         s = spec
         self.pool = pkv.KVPool(s.num_layers, placement.num_blocks, s.block_size, s.num_kv_heads,
-                               s.head_dim, s.torch_dtype, device=dev)
+                               s.head_dim, s.cache_torch_dtype, device=dev)
         self.tables = torch.from_numpy(placement.block_tables).to(dev)
         self.ctx = torch.from_numpy(placement.context_lens).to(dev)
         self.seq_ids = torch.from_numpy(newest_slot_masks(placement)).to(dev)
@@ -153,15 +184,17 @@ class LargeCase:
         kc, vc, q, kn, vn = self.fill(layer)
         used, ctab = compact_blocks(pl.block_tables, seqs)
         used_t = torch.from_numpy(used.astype(np.int64)).to(self.dev)
-        k_pre, v_pre = kc[used_t].cpu(), vc[used_t].cpu()  # the oracle's pool: pre-append
+        k_pre, v_pre = take(kc, used_t).cpu(), take(vc, used_t).cpu()  # the oracle's pool: pre-append
+        so = scale_opts(s)
         if fused:
             out32, slots = attend_append(q, kn, vn, kc, vc, self.tables, self.ctx, s.attn_scale,
-                                         seq_ids=self.seq_ids, out_dtype=torch.float32, **opts)
+                                         seq_ids=self.seq_ids, out_dtype=torch.float32, **so, **opts)
         else:
             slots = pkv.slot_mapping(self.tables, self.ctx, s.block_size, pl.num_blocks)
-            self.pool.append(layer, kn, vn, slots, seq_ids=self.seq_ids)
-            out32 = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, out_dtype=torch.float32, **opts)
-        outq = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, **opts)
+            self.pool.append(layer, kn, vn, slots, seq_ids=self.seq_ids, **so)
+            out32 = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, out_dtype=torch.float32,
+                           **so, **opts)
+        outq = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, **so, **opts)
         st, flags = pkv.device_status()
         assert st == 0 and flags == 0, f"device status {st} flags {flags:#x}"
         # Oracle on the sampled sequences, over the compact pool.
@@ -169,11 +202,11 @@ class LargeCase:
         o_sl = oracle.slot_mapping(ctab, ctx_s, s.block_size)
         o_sl = np.where(pl.appends[seqs], o_sl, -1).astype(np.int32)
         kn_s, vn_s, q_s = kn[seqs].cpu(), vn[seqs].cpu(), q[seqs].cpu()
-        k_post, v_post = oracle.append(k_pre, v_pre, kn_s, vn_s, o_sl)
-        ref = oracle.paged_decode(q_s, k_post, v_post, ctab, ctx_s, s.attn_scale)
+        k_post, v_post = oracle_append(s, k_pre, v_pre, kn_s, vn_s, o_sl)
+        ref = oracle_attention(s, q_s, k_post, v_post, ctab, ctx_s)
         # Append: every sampled block bit-exact after the step.
-        assert torch.equal(bits(kc[used_t].cpu()), bits(k_post)), "K blocks after append"
-        assert torch.equal(bits(vc[used_t].cpu()), bits(v_post)), "V blocks after append"
+        assert torch.equal(cache_bits(take(kc, used_t).cpu()), cache_bits(k_post)), "K blocks after append"
+        assert torch.equal(cache_bits(take(vc, used_t).cpu()), cache_bits(v_post)), "V blocks after append"
         # Device slot mapping: bit-exact for the sampled sequences (real table).
         o_full = oracle.slot_mapping(pl.block_tables[seqs], ctx_s, s.block_size)
         assert np.array_equal(slots.cpu().numpy()[seqs], o_full), "slot mapping"

@@ -19,8 +19,9 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+                "e4m3": torch.float8_e4m3fn}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
 
 
 @dataclass(frozen=True)
@@ -47,6 +48,11 @@ class WorkloadSpec:
     prefix_tokens: int = 0  # >0: groups of `prefix_group` sequences share this prefix
     prefix_group: int = 8
     scale: float = 0.0  # 0: 1/sqrt(head_dim)
+    # Cache storage type when it differs from `dtype` ("e4m3": an FP8 cache
+    # whose codes stand for kv_scales[0] (K) and kv_scales[1] (V) times their
+    # values; q and the new rows stay in `dtype`).
+    kv_dtype: str = ""
+    kv_scales: tuple = (1.0, 1.0)
 
     @property
     def group_size(self) -> int:
@@ -63,6 +69,22 @@ class WorkloadSpec:
     @property
     def torch_dtype(self) -> torch.dtype:
         return TORCH_DTYPES[self.dtype]
+
+    @property
+    def cache_dtype(self) -> str:
+        return self.kv_dtype or self.dtype
+
+    @property
+    def cache_torch_dtype(self) -> torch.dtype:
+        return TORCH_DTYPES[self.cache_dtype]
+
+    @property
+    def cache_elem_bytes(self) -> int:
+        return ELEM_BYTES[self.cache_dtype]
+
+    @property
+    def fp8(self) -> bool:
+        return self.cache_dtype == "e4m3"
 
 
 SPECS = {
@@ -94,6 +116,14 @@ SPECS = {
         num_kv_heads=8, head_dim=128, block_size=32, dtype="bf16", seed=4,
         ctx_dist="lognormal", lognormal_median=2048.0, lognormal_sigma=1.0,
         ctx_max=32768, pool_rule="ninety_percent_used"),
+    # The batch-32 step with an FP8 (E4M3) cache: K codes ~ N(0, 56^2) and V
+    # codes ~ N(0, 44^2) rounded to E4M3, scales 1/56 and 1/44, so the cached
+    # values are N(0, 1) draws at E4M3 precision.
+    "llama8b_32l_b32_fp8": WorkloadSpec(
+        name="llama8b_32l_b32_fp8", num_layers=32, num_seqs=32, num_q_heads=32,
+        num_kv_heads=8, head_dim=128, block_size=16, dtype="bf16", seed=2,
+        ctx_dist="const", ctx_const=4096, pool_rule="twice_used",
+        kv_dtype="e4m3", kv_scales=(1.0 / 56.0, 1.0 / 44.0)),
 }
 
 
@@ -227,25 +257,35 @@ def value_seed(spec: WorkloadSpec, layer: int, kind: int) -> int:
     return spec.seed * 1_000_003 + layer * 16 + kind
 
 
+def _sigma(spec: WorkloadSpec, kind: int) -> float:
+    """Standard deviation of the stored values: 1, or 1 / scale for E4M3 codes."""
+    return 1.0 / spec.kv_scales[kind - 1] if spec.fp8 else 1.0
+
+
 def pool_layer_values(spec: WorkloadSpec, num_blocks: int, layer: int, device="cpu"):
     """Pre-step contents of one layer's K and V pools: [NB, Hkv, bs, D] each."""
     shape = (num_blocks, spec.num_kv_heads, spec.block_size, spec.head_dim)
-    k = _normal(shape, spec.torch_dtype, value_seed(spec, layer, 1), device)
-    v = _normal(shape, spec.torch_dtype, value_seed(spec, layer, 2), device)
+    k = torch.empty(shape, dtype=spec.cache_torch_dtype, device=device)
+    v = torch.empty(shape, dtype=spec.cache_torch_dtype, device=device)
+    fill_pool_layer(spec, layer, k, v)
     return k, v
 
 
 def fill_pool_layer(spec: WorkloadSpec, layer: int, k_view: torch.Tensor, v_view: torch.Tensor):
-    """Same draw as pool_layer_values, written into existing [NB, Hkv, bs, D] views."""
+    """One layer's pool contents, written into existing [NB, Hkv, bs, D] views:
+    N(0, sigma^2) fp32 draws rounded to the cache type by torch's own cast."""
     for view, kind in ((k_view, 1), (v_view, 2)):
         flat = view.reshape(-1)
         g = _gen(value_seed(spec, layer, kind), view.device)
+        sigma = _sigma(spec, kind)
         n = flat.numel()
         step = 1 << 26
         for a in range(0, n, step):
             b = min(n, a + step)
-            flat[a:b] = torch.randn(b - a, generator=g, dtype=torch.float32,
-                                    device=view.device).to(view.dtype)
+            x = torch.randn(b - a, generator=g, dtype=torch.float32, device=view.device)
+            if sigma != 1.0:
+                x = x * sigma
+            flat[a:b] = x.to(view.dtype)
 
 
 def step_layer_values(spec: WorkloadSpec, num_seqs: int, layer: int, device="cpu"):
@@ -261,14 +301,15 @@ def step_layer_values(spec: WorkloadSpec, num_seqs: int, layer: int, device="cpu
 
 def small_spec(name="custom", *, num_q_heads=4, num_kv_heads=2, head_dim=64,
                block_size=16, dtype="f32", seed=11, ctx=(1, 15, 16, 17, 33),
-               num_blocks=0, scale=0.0) -> WorkloadSpec:
+               num_blocks=0, scale=0.0, kv_dtype="", kv_scales=(1.0, 1.0)) -> WorkloadSpec:
     """A small spec with explicit lengths, for edge-case tests."""
     ctx = tuple(int(c) for c in ctx)
     need = sum((c + block_size - 1) // block_size for c in ctx)
     return WorkloadSpec(name=name, num_layers=1, num_seqs=len(ctx), num_q_heads=num_q_heads,
                         num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size,
                         dtype=dtype, seed=seed, ctx_dist="list", ctx_list=ctx,
-                        num_blocks=num_blocks or max(1, 2 * need), scale=scale)
+                        num_blocks=num_blocks or max(1, 2 * need), scale=scale,
+                        kv_dtype=kv_dtype, kv_scales=tuple(kv_scales))
 
 
 def prefix_request_trace(seed: int, num_ops: int, *, num_prompts: int = 6, vocab: int = 50,
