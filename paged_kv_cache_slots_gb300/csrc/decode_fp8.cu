@@ -7,6 +7,9 @@
 // registers (two codes per conversion) and fed to the f16 m16n8k16 MMA:
 //   S^T = K8 . Q^T           scores, times scale * log2(e) * k_scale
 //   O^T += V8^T . P^T        times v_scale when the state is written out
+// P enters the PV product as an f16 high part plus an f16 low part; with up
+// to 4 query heads per KV head the low parts ride in the MMA's padding
+// columns 4-7 (one PV MMA per 16-dim slice), folded back when written out.
 // q (f16 or bf16) becomes f16 B fragments once per (sequence, head).
 //
 // Fragment layout.  ldmatrix moves 16-bit elements, i.e. pairs of codes.
@@ -29,56 +32,129 @@
 
 namespace pkv {
 
-template <int QT, int D>
+// kQ8: QK on the E4M3 tensor path (bf16 q, at most 4 query heads per KV
+// head).  The K tile feeds the m16n8k32 E4M3 MMA straight from ldmatrix (a
+// lane's four consecutive codes are exactly its A-fragment bytes), so K needs
+// no conversion.  q is scaled per head by a power of two 2^kq (largest |q| to
+// [128, 256)) and split exactly into two E4M3 parts, hi = RN(q') and
+// lo = q' - hi (a bf16 value has 8 significant bits, each part holds 4, and
+// the rounding residual of hi is a multiple of hi's last-bit weight / 16 no
+// larger than half of it, so it fits 4 bits): columns 0-3 carry hi and
+// columns 4-7 lo of heads col % G, and the two halves of each score are
+// added with one shuffle.  Scores then carry scale * log2(e) * k_scale * 2^-kq.
+template <int QT, int D, bool kQ8 = false>
 struct MmaFp8Policy {
     static_assert(D == 128, "E4M3 rows of 128 codes: one 128-byte slice per row");
+    static_assert(!kQ8 || QT == kBF16, "the E4M3 QK path splits a bf16 q exactly");
     static constexpr bool kTensor = true;
     static constexpr bool kScratch = false;
     static constexpr int KS = D / 16;  // 16-dim chunks: k-slices of QK, m-slices of PV
+    static constexpr int K8 = D / 32;  // 32-dim k-slices of the E4M3 QK
     static constexpr int kD = D;
     using T = typename Elem<QT>::T;
 
     struct State {
-        uint32_t qb[KS][2];  // f16 B fragments of Q^T, head lane/4: dims 16ks + 4(lane%4) + {0,1} / {2,3}
+        // f16 B fragments of Q^T, head lane/4: dims 16ks + 4(lane%4) + {0,1} / {2,3};
+        // kQ8: E4M3 B fragments, dims 32j + 4(lane%4) + {0..3} / 16 + ...
+        uint32_t qb[kQ8 ? K8 : KS][2];
+        float sc[2];         // kQ8: score multipliers of columns 2(lane%4), 2(lane%4)+1
         float o[KS][4];      // O^T: dims 16mi + 2(lane/4) (+1 for [2],[3]), heads 2(lane%4) (+1 for [1],[3])
         float m[2];          // running max of heads 2(lane%4), 2(lane%4)+1
         float l[2];          // this lane's share of the running sum
     };
 
-    __device__ __forceinline__ void begin(State& st, const DecodeArgs& a, int s, int h, int G) {
+    // kQ8 begin: B fragments of q's two E4M3 parts and the per-column score scale.
+    __device__ __forceinline__ void begin_q8(State& st, const DecodeArgs& a, int s, int h, int G) {
         const int lane = threadIdx.x & 31;
         const int g = lane >> 2, c = lane & 3;
         const T* q = static_cast<const T*>(a.q) +
-                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D;
+                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g % G) * D;
+        float v[K8][8];
+        float mx = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            if (g < G) {
-                const uint2 raw = *reinterpret_cast<const uint2*>(q + 16 * ks + 4 * c);
-                if constexpr (QT == kF16) {
-                    st.qb[ks][0] = raw.x;
-                    st.qb[ks][1] = raw.y;
-                } else {
-                    const T* e = reinterpret_cast<const T*>(&raw);
-                    const __half2 h0 = __floats2half2_rn(Elem<QT>::to_float(e[0]), Elem<QT>::to_float(e[1]));
-                    const __half2 h1 = __floats2half2_rn(Elem<QT>::to_float(e[2]), Elem<QT>::to_float(e[3]));
-                    st.qb[ks][0] = *reinterpret_cast<const uint32_t*>(&h0);
-                    st.qb[ks][1] = *reinterpret_cast<const uint32_t*>(&h1);
+        for (int j = 0; j < K8; ++j) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint2 raw = *reinterpret_cast<const uint2*>(q + 32 * j + 16 * half + 4 * c);
+                const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[j][4 * half + i] = Elem<QT>::to_float(e[i]);
+                    mx = fmaxf(mx, fabsf(v[j][4 * half + i]));
                 }
-            } else {
-                st.qb[ks][0] = 0u;
-                st.qb[ks][1] = 0u;
             }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // 2^kq with mx * 2^kq in [128, 256): kq = 7 - floor(log2 mx).
+        int kq = 0;
+        if (mx > 0.f) kq = 7 - (((__float_as_int(mx) >> 23) & 0xff) - 127);
+        kq = kq < -120 ? -120 : (kq > 120 ? 120 : kq);
+        const float up = __int_as_float((127 + kq) << 23);
+        const bool lo_part = g >= 4;
+#pragma unroll
+        for (int j = 0; j < K8; ++j) {
+            uint32_t w[2];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t word = 0u;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const float x0 = v[j][4 * half + 2 * p] * up, x1 = v[j][4 * half + 2 * p + 1] * up;
+                    const uint16_t hi = e4m3x2_from_floats(x0, x1);
+                    const uint32_t hh = e4m3x2_to_half2(hi);
+                    const __half2 hd = *reinterpret_cast<const __half2*>(&hh);
+                    const uint16_t lo = e4m3x2_from_floats(x0 - __low2float(hd), x1 - __high2float(hd));
+                    word |= static_cast<uint32_t>(lo_part ? lo : hi) << (16 * p);
+                }
+                w[half] = word;
+            }
+            st.qb[j][0] = w[0];
+            st.qb[j][1] = w[1];
+        }
+        const int k0 = __shfl_sync(0xffffffffu, kq, 8 * c);      // column 2c's head sits in lane 4 * 2c
+        const int k1 = __shfl_sync(0xffffffffu, kq, 8 * c + 4);  // column 2c+1
+        st.sc[0] = a.scale_log2 * __int_as_float((127 - k0) << 23);
+        st.sc[1] = a.scale_log2 * __int_as_float((127 - k1) << 23);
+    }
+
+    __device__ __forceinline__ void begin(State& st, const DecodeArgs& a, int s, int h, int G) {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
             for (int r = 0; r < 4; ++r) st.o[ks][r] = 0.f;
-        }
         st.m[0] = st.m[1] = -INFINITY;
         st.l[0] = st.l[1] = 0.f;
+        if constexpr (kQ8) {
+            begin_q8(st, a, s, h, G);
+            return;
+        }
+        const int g = lane >> 2, c = lane & 3;
+        // Columns g >= G (padding of the MMA's 8 columns) repeat head g % G,
+        // so their scores and probabilities equal that head's (see tile()).
+        const T* q = static_cast<const T*>(a.q) +
+                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g % G) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(q + 16 * ks + 4 * c);
+            if constexpr (QT == kF16) {
+                st.qb[ks][0] = raw.x;
+                st.qb[ks][1] = raw.y;
+            } else {
+                const T* e = reinterpret_cast<const T*>(&raw);
+                const __half2 h0 = __floats2half2_rn(Elem<QT>::to_float(e[0]), Elem<QT>::to_float(e[1]));
+                const __half2 h1 = __floats2half2_rn(Elem<QT>::to_float(e[2]), Elem<QT>::to_float(e[3]));
+                st.qb[ks][0] = *reinterpret_cast<const uint32_t*>(&h0);
+                st.qb[ks][1] = *reinterpret_cast<const uint32_t*>(&h1);
+            }
+        }
     }
 
     // One head's part of a stage: kt/vt point at the stage's K/V codes,
     // [Hc*bs rows][128 B]; this warp's head owns rows hw*bs .. hw*bs+bs-1.
     __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, uint8_t* kt, uint8_t* vt,
-                                         int hw, int n_valid, int, float*) {
+                                         int hw, int n_valid, int G, float*) {
         const int lane = threadIdx.x & 31;
         const int bs = a.block_size;
         uint8_t* kh = kt + hw * bs * 128;
@@ -101,29 +177,49 @@ struct MmaFp8Policy {
         const uint32_t csel = static_cast<uint32_t>(lane >> 4);
         for (int mt = 0; mt < bs / 16; ++mt) {
             const uint32_t row = static_cast<uint32_t>(mt * 16) + rsel;
-            // ---- S^T = K . Q^T for tokens 16mt .. 16mt+15
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- S^T = K . Q^T for tokens 16mt .. 16mt+15.  The warp-level MMA
+            // has a long latency, so the 8 chunks accumulate into 4 independent
+            // chains that are summed at the end.
+            float part[4][4];
 #pragma unroll
             for (int kp = 0; kp < KS / 2; ++kp) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) part[kp][r] = 0.f;
                 uint32_t r[4];
                 ldsm_x4(r, kb + row * 128u + ((((2u * kp) | csel) ^ sw) << 4));
+                if constexpr (kQ8) {
+                    // r[0] / r[1]: rows g / g+8, dims 32kp + 4c..; r[2] / r[3]: dims 32kp + 16 + 4c..
+                    const uint32_t af[4] = {r[0], r[1], r[2], r[3]};
+                    mma16832_e4m3(part[kp], af, st.qb[kp][0], st.qb[kp][1]);
+                } else {
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {  // chunk 2kp + hf: rows g / g+8 in r[2hf] / r[2hf+1]
-                    uint32_t af[4];
-                    af[0] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf]));
-                    af[1] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1]));
-                    af[2] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf] >> 16));
-                    af[3] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1] >> 16));
-                    mma16816<kF16>(acc, af, st.qb[2 * kp + hf][0], st.qb[2 * kp + hf][1]);
+                    for (int hf = 0; hf < 2; ++hf) {  // chunk 2kp + hf: rows g / g+8 in r[2hf] / r[2hf+1]
+                        uint32_t af[4];
+                        af[0] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf]));
+                        af[1] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1]));
+                        af[2] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf] >> 16));
+                        af[3] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1] >> 16));
+                        mma16816<kF16>(part[kp], af, st.qb[2 * kp + hf][0], st.qb[2 * kp + hf][1]);
+                    }
                 }
+            }
+            float acc[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[r] = (part[0][r] + part[1][r]) + (part[2][r] + part[3][r]);
+            float sl0 = sl, sl1 = sl;
+            if constexpr (kQ8) {  // hi (columns < 4) + lo (columns >= 4) of the same head
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 2);
+                sl0 = st.sc[0];
+                sl1 = st.sc[1];
             }
             // ---- online softmax (heads 2c, 2c+1; tokens g and g+8 of the slice)
             const int t0 = mt * 16 + (lane >> 2);
             const bool v0 = t0 < n_valid, v1 = t0 + 8 < n_valid;
-            const float x0 = v0 ? acc[0] * sl : -INFINITY;
-            const float x1 = v0 ? acc[1] * sl : -INFINITY;
-            const float x2 = v1 ? acc[2] * sl : -INFINITY;
-            const float x3 = v1 ? acc[3] * sl : -INFINITY;
+            const float x0 = v0 ? acc[0] * sl0 : -INFINITY;
+            const float x1 = v0 ? acc[1] * sl1 : -INFINITY;
+            const float x2 = v1 ? acc[2] * sl0 : -INFINITY;
+            const float x3 = v1 ? acc[3] * sl1 : -INFINITY;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off <= 16; off <<= 1) {
@@ -147,12 +243,20 @@ struct MmaFp8Policy {
                     st.o[mi][3] *= al1;
                 }
             }
-            // ---- P^T fragments (k = token, n = head), f16 high + low parts
+            // ---- P^T fragments (k = token, n = head), f16 high + low parts; with
+            // G <= 4 the low parts ride in the padding columns 4-7 (see emit).
             uint32_t h01, l01, h23, l23;
             pack_split<kF16>(p0, p1, h01, l01);
             pack_split<kF16>(p2, p3, h23, l23);
-            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-            const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+            const bool packed = kQ8 || G <= 4;
+            const bool lo_cols = (lane & 3) >= 2;
+            const uint32_t bh0 = movmatrix_trans(packed && lo_cols ? l01 : h01);
+            const uint32_t bh1 = movmatrix_trans(packed && lo_cols ? l23 : h23);
+            uint32_t bl0 = 0u, bl1 = 0u;
+            if (!packed) {
+                bl0 = movmatrix_trans(l01);
+                bl1 = movmatrix_trans(l23);
+            }
             // ---- O^T += V^T . P^T
 #pragma unroll
             for (int mp = 0; mp < KS / 2; ++mp) {
@@ -170,7 +274,7 @@ struct MmaFp8Policy {
                     af[2] = e4m3x2_to_half2(static_cast<uint16_t>(hi));        // dim 2g,   tokens 8+2c, 9+2c
                     af[3] = e4m3x2_to_half2(static_cast<uint16_t>(hi >> 16));  // dim 2g+1, tokens 8+2c, 9+2c
                     mma16816<kF16>(st.o[2 * mp + hf], af, bh0, bh1);
-                    mma16816<kF16>(st.o[2 * mp + hf], af, bl0, bl1);
+                    if (!packed) mma16816<kF16>(st.o[2 * mp + hf], af, bl0, bl1);
                 }
             }
         }
@@ -182,6 +286,16 @@ struct MmaFp8Policy {
                                                 uint4 val) const {
         const int row = hw * a.block_size + r;
         *reinterpret_cast<uint4*>(t + row * 128 + (((q & 7) ^ (row & 7)) << 4)) = val;
+    }
+
+    // Accumulators of slice mi with the low-part columns (4-7, G <= 4) added
+    // to the columns of their heads; valid in lanes whose columns are < 4.
+    __device__ __forceinline__ void fold(const State& st, int mi, int G, float (&v)[4]) const {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float other = __shfl_down_sync(0xffffffffu, st.o[mi][r], 2);
+            v[r] = st.o[mi][r] + (G <= 4 ? other : 0.f);
+        }
     }
 
     __device__ __forceinline__ void row_sums(const State& st, float& l0, float& l1) const {
@@ -204,14 +318,16 @@ struct MmaFp8Policy {
         const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
         for (int mi = 0; mi < KS; ++mi) {
+            float v[4];
+            fold(st, mi, G, v);
             const int d0 = 16 * mi + 2 * g;
             if (h0 < G) {
-                o[h0 * os + d0] = st.o[mi][0] * vs;
-                o[h0 * os + d0 + 1] = st.o[mi][2] * vs;
+                o[h0 * os + d0] = v[0] * vs;
+                o[h0 * os + d0 + 1] = v[2] * vs;
             }
             if (h1 < G) {
-                o[h1 * os + d0] = st.o[mi][1] * vs;
-                o[h1 * os + d0 + 1] = st.o[mi][3] * vs;
+                o[h1 * os + d0] = v[1] * vs;
+                o[h1 * os + d0 + 1] = v[3] * vs;
             }
         }
         if (g == 0) {
@@ -248,14 +364,16 @@ struct MmaFp8Policy {
         const int64_t base = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
 #pragma unroll
         for (int mi = 0; mi < KS; ++mi) {
+            float v[4];
+            fold(st, mi, G, v);
             const int d0 = 16 * mi + 2 * g;
             if (h0 < G) {
-                store_out(a.out, base + h0 * D + d0, st.o[mi][0] * i0, a.out_dtype);
-                store_out(a.out, base + h0 * D + d0 + 1, st.o[mi][2] * i0, a.out_dtype);
+                store_out(a.out, base + h0 * D + d0, v[0] * i0, a.out_dtype);
+                store_out(a.out, base + h0 * D + d0 + 1, v[2] * i0, a.out_dtype);
             }
             if (h1 < G) {
-                store_out(a.out, base + h1 * D + d0, st.o[mi][1] * i1, a.out_dtype);
-                store_out(a.out, base + h1 * D + d0 + 1, st.o[mi][3] * i1, a.out_dtype);
+                store_out(a.out, base + h1 * D + d0, v[1] * i1, a.out_dtype);
+                store_out(a.out, base + h1 * D + d0 + 1, v[3] * i1, a.out_dtype);
             }
         }
     }
@@ -264,7 +382,9 @@ struct MmaFp8Policy {
 cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                               cudaStream_t stream) {
     if (a.kv_dtype != kFP8 || a.head_dim != 128) return cudaErrorInvalidValue;
+    const int G = a.num_q_heads / a.num_kv_heads;
     if (a.dtype == kF16) return launch_partial<MmaFp8Policy<kF16, 128>>(a, tmk, tmv, stream);
+    if (a.dtype == kBF16 && G <= 4) return launch_partial<MmaFp8Policy<kBF16, 128, true>>(a, tmk, tmv, stream);
     if (a.dtype == kBF16) return launch_partial<MmaFp8Policy<kBF16, 128>>(a, tmk, tmv, stream);
     return cudaErrorInvalidValue;
 }

@@ -516,10 +516,12 @@ __global__ void __launch_bounds__(32 * 16, 1)
         const int ctx = clamp_context(a, s, false);
         pol.begin(st, a, s, h, G);
         const int first = seg + (((rr - (seg - start)) % R) + R) % R;
+        // Ring position of item `first` (item t = i - start sits in stage
+        // t % stages, phase (t / stages) & 1); advanced by R per item below.
+        int stage = (first - start) % a.stages;
+        uint32_t phase = static_cast<uint32_t>((first - start) / a.stages) & 1u;
         for (int i = first; i < seg_end; i += R) {
-            const int t = i - start;
-            const int stage = t % a.stages;
-            const bool ok = mbar_wait_bounded(&full[stage], (t / a.stages) & 1, abort, a.status);
+            const bool ok = mbar_wait_bounded(&full[stage], phase, abort, a.status);
             if (ok) {
                 const int j = i - pair_a;
                 const int n_valid = min(a.block_size, ctx - j * a.block_size);
@@ -530,6 +532,11 @@ __global__ void __launch_bounds__(32 * 16, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
+            stage += R;  // R divides the ring size, so this wraps exactly at the end
+            if (stage >= a.stages) {
+                stage -= a.stages;
+                phase ^= 1u;
+            }
         }
         const bool whole = (pair_a >= start) && (pair_b <= end);
         const int pair = s * chunks + hc;

@@ -11,7 +11,9 @@
 // the N dimension (padded to 8) and q stays in registers as B fragments.
 // P^T is formed from the score accumulators with movmatrix (transpose in
 // registers) and split into a high and a low half-precision part, so the
-// probabilities carry ~16 significant bits into the PV product.
+// probabilities carry ~16 significant bits into the PV product.  With up to
+// 4 query heads per KV head the low parts travel in the padding columns 4-7
+// of the same MMA (one PV MMA per slice instead of two).
 // K and V tiles arrive through 2-D tensor maps with a 128-byte swizzle, which
 // makes the eight 16-byte rows of every ldmatrix fall in distinct banks.
 #include "decode_kernel.cuh"
@@ -37,17 +39,14 @@ struct MmaPolicy {
     __device__ __forceinline__ void begin(State& st, const DecodeArgs& a, int s, int h, int G) {
         const int lane = threadIdx.x & 31;
         const int g = lane >> 2, c = lane & 3;
+        // Columns g >= G (padding of the MMA's 8 columns) repeat head g % G,
+        // so their scores and probabilities equal that head's (see tile()).
         const T* q = static_cast<const T*>(a.q) +
-                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g) * D;
+                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g % G) * D;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            if (g < G) {
-                st.qb[ks][0] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * c);
-                st.qb[ks][1] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * c + 8);
-            } else {
-                st.qb[ks][0] = 0u;
-                st.qb[ks][1] = 0u;
-            }
+            st.qb[ks][0] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * c);
+            st.qb[ks][1] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * c + 8);
 #pragma unroll
             for (int r = 0; r < 4; ++r) st.o[ks][r] = 0.f;
         }
@@ -59,7 +58,7 @@ struct MmaPolicy {
     // [64-element slice][Hc*bs rows][128 B] (128-byte swizzled by the tensor
     // copy); this warp's head owns rows hw*bs .. hw*bs+bs-1 of every slice.
     __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, uint8_t* kt, uint8_t* vt,
-                                         int hw, int n_valid, int, float*) {
+                                         int hw, int n_valid, int G, float*) {
         const int lane = threadIdx.x & 31;
         const int bs = a.block_size;
         const uint32_t slice_bytes = static_cast<uint32_t>(a.heads_per_stage * bs) * 128u;
@@ -82,8 +81,15 @@ struct MmaPolicy {
         const uint32_t sw = lane & 7;  // 128-byte swizzle key of the rows this lane addresses
         const float sl = a.scale_log2;
         for (int mt = 0; mt < bs / 16; ++mt) {
-            // ---- S^T = K . Q^T for tokens 16mt .. 16mt+15
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- S^T = K . Q^T for tokens 16mt .. 16mt+15.  The warp-level MMA
+            // has a long latency: the k-steps accumulate into up to 4
+            // independent chains, summed at the end.
+            constexpr int NC = KS < 4 ? KS : 4;
+            float part[NC][4];
+#pragma unroll
+            for (int k = 0; k < NC; ++k)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) part[k][r] = 0.f;
             {
                 const uint32_t row = static_cast<uint32_t>(mt * 16 + (lane & 7) + (lane & 8));
 #pragma unroll
@@ -91,8 +97,15 @@ struct MmaPolicy {
                     const uint32_t chunk = ((ks & 3) << 1) | (lane >> 4);
                     uint32_t af[4];
                     ldsm_x4(af, kb + (ks >> 2) * slice_bytes + row * 128u + ((chunk ^ sw) << 4));
-                    mma16816<DT>(acc, af, st.qb[ks][0], st.qb[ks][1]);
+                    mma16816<DT>(part[ks % NC], af, st.qb[ks][0], st.qb[ks][1]);
                 }
+            }
+            float acc[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                acc[r] = part[0][r];
+#pragma unroll
+                for (int k = 1; k < NC; ++k) acc[r] += part[k][r];
             }
             // ---- online softmax (heads 2c, 2c+1; tokens g and g+8 of the slice)
             const int t0 = mt * 16 + (lane >> 2);
@@ -124,12 +137,22 @@ struct MmaPolicy {
                     st.o[mi][3] *= al1;
                 }
             }
-            // ---- P^T fragments (k = token, n = head), high + low parts
+            // ---- P^T fragments (k = token, n = head), high + low parts.  With
+            // G <= 4 the low parts ride in columns 4-7 (which repeat heads 0-3,
+            // so this lane's probabilities there are those of head col % G):
+            // one MMA per slice; O of head h is then column h + column h + 4.
             uint32_t h01, l01, h23, l23;
             pack_split<DT>(p0, p1, h01, l01);
             pack_split<DT>(p2, p3, h23, l23);
-            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-            const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+            const bool packed = G <= 4;
+            const bool lo_cols = (lane & 3) >= 2;  // this lane's columns 2c, 2c+1 are >= 4
+            const uint32_t bh0 = movmatrix_trans(packed && lo_cols ? l01 : h01);
+            const uint32_t bh1 = movmatrix_trans(packed && lo_cols ? l23 : h23);
+            uint32_t bl0 = 0u, bl1 = 0u;
+            if (!packed) {
+                bl0 = movmatrix_trans(l01);
+                bl1 = movmatrix_trans(l23);
+            }
             // ---- O^T += V^T . P^T
             {
                 const uint32_t row = static_cast<uint32_t>(mt * 16 + (lane & 7) + ((lane >> 4) << 3));
@@ -140,7 +163,7 @@ struct MmaPolicy {
                     uint32_t af[4];
                     ldsm_x4_trans(af, vb + (mi >> 2) * slice_bytes + row * 128u + ((chunk ^ sw) << 4));
                     mma16816<DT>(st.o[mi], af, bh0, bh1);
-                    mma16816<DT>(st.o[mi], af, bl0, bl1);
+                    if (!packed) mma16816<DT>(st.o[mi], af, bl0, bl1);
                 }
             }
         }
@@ -155,6 +178,16 @@ struct MmaPolicy {
         const int slice_bytes = a.heads_per_stage * bs * 128;
         const int row = hw * bs + r;
         *reinterpret_cast<uint4*>(t + (q >> 3) * slice_bytes + row * 128 + (((q & 7) ^ (row & 7)) << 4)) = val;
+    }
+
+    // Accumulators of slice mi with the low-part columns (4-7, G <= 4) added
+    // to the columns of their heads; valid in lanes whose columns are < 4.
+    __device__ __forceinline__ void fold(const State& st, int mi, int G, float (&v)[4]) const {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float other = __shfl_down_sync(0xffffffffu, st.o[mi][r], 2);
+            v[r] = st.o[mi][r] + (G <= 4 ? other : 0.f);
+        }
     }
 
     // Row sums of heads 2c, 2c+1 over the whole warp.
@@ -178,14 +211,16 @@ struct MmaPolicy {
         const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
         for (int mi = 0; mi < KS; ++mi) {
+            float v[4];
+            fold(st, mi, G, v);
             const int d0 = 16 * mi + g;
             if (h0 < G) {
-                o[h0 * os + d0] = st.o[mi][0];
-                o[h0 * os + d0 + 8] = st.o[mi][2];
+                o[h0 * os + d0] = v[0];
+                o[h0 * os + d0 + 8] = v[2];
             }
             if (h1 < G) {
-                o[h1 * os + d0] = st.o[mi][1];
-                o[h1 * os + d0 + 8] = st.o[mi][3];
+                o[h1 * os + d0] = v[1];
+                o[h1 * os + d0 + 8] = v[3];
             }
         }
         if (g == 0) {
@@ -222,14 +257,16 @@ struct MmaPolicy {
         const int64_t base = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
 #pragma unroll
         for (int mi = 0; mi < KS; ++mi) {
+            float v[4];
+            fold(st, mi, G, v);
             const int d0 = 16 * mi + g;
             if (h0 < G) {
-                store_out(a.out, base + h0 * D + d0, st.o[mi][0] * i0, a.out_dtype);
-                store_out(a.out, base + h0 * D + d0 + 8, st.o[mi][2] * i0, a.out_dtype);
+                store_out(a.out, base + h0 * D + d0, v[0] * i0, a.out_dtype);
+                store_out(a.out, base + h0 * D + d0 + 8, v[2] * i0, a.out_dtype);
             }
             if (h1 < G) {
-                store_out(a.out, base + h1 * D + d0, st.o[mi][1] * i1, a.out_dtype);
-                store_out(a.out, base + h1 * D + d0 + 8, st.o[mi][3] * i1, a.out_dtype);
+                store_out(a.out, base + h1 * D + d0, v[1] * i1, a.out_dtype);
+                store_out(a.out, base + h1 * D + d0 + 8, v[3] * i1, a.out_dtype);
             }
         }
     }

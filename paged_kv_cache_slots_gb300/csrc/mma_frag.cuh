@@ -44,6 +44,19 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
     }
 }
 
+// D += A . B with E4M3 operands: A 16x32 (row), B 32x8 (col), fp32 accumulators.
+// A register holds 4 codes of consecutive k (lowest k in the low byte): a0/a2
+// rows g, a1/a3 rows g+8, k 4c..4c+3 (a0, a1) and 16+4c.. (a2, a3); b0 / b1
+// hold k 4c.. / 16+4c.. of column g (g = lane / 4, c = lane % 4).
+__device__ __forceinline__ void mma16832_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Pack two fp32 values (lower column first) and the residual of the rounding.
 template <int DT>
 __device__ __forceinline__ void pack_split(float x0, float x1, uint32_t& hi, uint32_t& lo) {

@@ -124,6 +124,13 @@ SPECS = {
         num_kv_heads=8, head_dim=128, block_size=16, dtype="bf16", seed=2,
         ctx_dist="const", ctx_const=4096, pool_rule="twice_used",
         kv_dtype="e4m3", kv_scales=(1.0 / 56.0, 1.0 / 44.0)),
+    # The serving mix with an FP8 cache (same lengths and placement rule).
+    "serving_b256_fp8": WorkloadSpec(
+        name="serving_b256_fp8", num_layers=32, num_seqs=256, num_q_heads=32,
+        num_kv_heads=8, head_dim=128, block_size=32, dtype="bf16", seed=4,
+        ctx_dist="lognormal", lognormal_median=2048.0, lognormal_sigma=1.0,
+        ctx_max=32768, pool_rule="ninety_percent_used",
+        kv_dtype="e4m3", kv_scales=(1.0 / 56.0, 1.0 / 44.0)),
 }
 
 
