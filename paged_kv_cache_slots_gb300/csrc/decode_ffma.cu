@@ -72,6 +72,7 @@ template <int DT, int D, int G>
 struct FfmaPolicy {
     static constexpr bool kTensor = false;
     static constexpr bool kScratch = true;
+    static constexpr bool kPairs = false;
     static constexpr int VD = D / 32;
     static constexpr int kD = D;
     using T = typename Elem<DT>::T;

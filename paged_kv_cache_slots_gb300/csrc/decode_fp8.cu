@@ -151,46 +151,44 @@ struct MmaFp8Policy {
         }
     }
 
-    // One head's part of a stage: kt/vt point at the stage's K/V codes,
-    // [Hc*bs rows][128 B]; this warp's head owns rows hw*bs .. hw*bs+bs-1.
-    __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, uint8_t* kt, uint8_t* vt,
-                                         int hw, int n_valid, int G, float*) {
+    // Rows past the valid tokens may hold any code (even NaN): zero this
+    // head's V rows [n_valid, bs) of a stage so that 0 * V stays 0 in PV.
+    __device__ __forceinline__ void zero_tail(uint8_t* vh, int n_valid, int bs) const {
         const int lane = threadIdx.x & 31;
-        const int bs = a.block_size;
-        uint8_t* kh = kt + hw * bs * 128;
-        uint8_t* vh = vt + hw * bs * 128;
-        // Rows past the valid tokens may hold any code (even NaN): zero this
-        // head's V rows there so that 0 * V stays 0 in the PV product.
-        if (n_valid < bs) {
-            for (int e = lane; e < (bs - n_valid) * 8; e += 32) {
-                uint4* p = reinterpret_cast<uint4*>(vh + (n_valid + (e >> 3)) * 128 + ((e & 7) << 4));
-                *p = make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncwarp();
+        for (int e = lane; e < (bs - n_valid) * 8; e += 32) {
+            uint4* p = reinterpret_cast<uint4*>(vh + (n_valid + (e >> 3)) * 128 + ((e & 7) << 4));
+            *p = make_uint4(0u, 0u, 0u, 0u);
         }
-        const uint32_t kb = smem_addr(kh), vb = smem_addr(vh);
+        __syncwarp();
+    }
+
+    // NS 16-token slices at once: kb[n] / vb[n] are the shared addresses of
+    // slice n's first K / V row, nv[n] its valid tokens (<= 0: none).  One
+    // online-softmax update covers all their tokens, and the independent MMA
+    // chains of the slices interleave, which keeps the warp's dependent
+    // instruction chains short.
+    template <int NS>
+    __device__ __forceinline__ void slices(State& st, const DecodeArgs& a, const uint32_t (&kb)[NS],
+                                           const uint32_t (&vb)[NS], const int (&nv)[NS], int G) {
+        const int lane = threadIdx.x & 31;
         const uint32_t sw = lane & 7;  // swizzle key of the rows this lane addresses
-        const float sl = a.scale_log2;
         // Lanes 0-7 / 8-15 / 16-23 / 24-31 address rows 0-7 / 8-15 / 0-7 / 8-15
-        // of the 16-token slice, in chunk 2p / 2p / 2p+1 / 2p+1.
-        const uint32_t rsel = static_cast<uint32_t>((lane & 7) + (lane & 8));
+        // of a slice, in chunk 2p / 2p / 2p+1 / 2p+1.
+        const uint32_t rofs = static_cast<uint32_t>((lane & 7) + (lane & 8)) * 128u;
         const uint32_t csel = static_cast<uint32_t>(lane >> 4);
-        for (int mt = 0; mt < bs / 16; ++mt) {
-            const uint32_t row = static_cast<uint32_t>(mt * 16) + rsel;
-            // ---- S^T = K . Q^T for tokens 16mt .. 16mt+15.  The warp-level MMA
-            // has a long latency, so the 8 chunks accumulate into 4 independent
-            // chains that are summed at the end.
-            float part[4][4];
+        // ---- S^T = K . Q^T, two accumulation chains per slice
+        float acc[NS][4];
+#pragma unroll
+        for (int n = 0; n < NS; ++n) {
+            float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int kp = 0; kp < KS / 2; ++kp) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) part[kp][r] = 0.f;
                 uint32_t r[4];
-                ldsm_x4(r, kb + row * 128u + ((((2u * kp) | csel) ^ sw) << 4));
+                ldsm_x4(r, kb[n] + rofs + ((((2u * kp) | csel) ^ sw) << 4));
                 if constexpr (kQ8) {
                     // r[0] / r[1]: rows g / g+8, dims 32kp + 4c..; r[2] / r[3]: dims 32kp + 16 + 4c..
                     const uint32_t af[4] = {r[0], r[1], r[2], r[3]};
-                    mma16832_e4m3(part[kp], af, st.qb[kp][0], st.qb[kp][1]);
+                    mma16832_e4m3(part[kp & 1], af, st.qb[kp][0], st.qb[kp][1]);
                 } else {
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {  // chunk 2kp + hf: rows g / g+8 in r[2hf] / r[2hf+1]
@@ -199,69 +197,83 @@ struct MmaFp8Policy {
                         af[1] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1]));
                         af[2] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf] >> 16));
                         af[3] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1] >> 16));
-                        mma16816<kF16>(part[kp], af, st.qb[2 * kp + hf][0], st.qb[2 * kp + hf][1]);
+                        mma16816<kF16>(part[hf], af, st.qb[2 * kp + hf][0], st.qb[2 * kp + hf][1]);
                     }
                 }
             }
-            float acc[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[r] = (part[0][r] + part[1][r]) + (part[2][r] + part[3][r]);
-            float sl0 = sl, sl1 = sl;
+            for (int r = 0; r < 4; ++r) acc[n][r] = part[0][r] + part[1][r];
             if constexpr (kQ8) {  // hi (columns < 4) + lo (columns >= 4) of the same head
 #pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 2);
-                sl0 = st.sc[0];
-                sl1 = st.sc[1];
+                for (int r = 0; r < 4; ++r) acc[n][r] += __shfl_xor_sync(0xffffffffu, acc[n][r], 2);
             }
-            // ---- online softmax (heads 2c, 2c+1; tokens g and g+8 of the slice)
-            const int t0 = mt * 16 + (lane >> 2);
-            const bool v0 = t0 < n_valid, v1 = t0 + 8 < n_valid;
-            const float x0 = v0 ? acc[0] * sl0 : -INFINITY;
-            const float x1 = v0 ? acc[1] * sl1 : -INFINITY;
-            const float x2 = v1 ? acc[2] * sl0 : -INFINITY;
-            const float x3 = v1 ? acc[3] * sl1 : -INFINITY;
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        }
+        const float sl0 = kQ8 ? st.sc[0] : a.scale_log2;
+        const float sl1 = kQ8 ? st.sc[1] : a.scale_log2;
+        // ---- online softmax over all NS slices (heads 2c, 2c+1; tokens g, g+8 of each)
+        float x[NS][4];
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int off = 4; off <= 16; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
-            const float al0 = fast_exp2(st.m[0] - mn0), al1 = fast_exp2(st.m[1] - mn1);
-            st.m[0] = mn0;
-            st.m[1] = mn1;
-            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
-            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
-            st.l[0] = st.l[0] * al0 + (p0 + p2);
-            st.l[1] = st.l[1] * al1 + (p1 + p3);
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+        for (int n = 0; n < NS; ++n) {
+            const int t0 = lane >> 2;
+            const bool v0 = t0 < nv[n], v1 = t0 + 8 < nv[n];
+            x[n][0] = v0 ? acc[n][0] * sl0 : -INFINITY;
+            x[n][1] = v0 ? acc[n][1] * sl1 : -INFINITY;
+            x[n][2] = v1 ? acc[n][2] * sl0 : -INFINITY;
+            x[n][3] = v1 ? acc[n][3] * sl1 : -INFINITY;
+            mx0 = fmaxf(mx0, fmaxf(x[n][0], x[n][2]));
+            mx1 = fmaxf(mx1, fmaxf(x[n][1], x[n][3]));
+        }
 #pragma unroll
-                for (int mi = 0; mi < KS; ++mi) {
-                    st.o[mi][0] *= al0;
-                    st.o[mi][1] *= al1;
-                    st.o[mi][2] *= al0;
-                    st.o[mi][3] *= al1;
-                }
-            }
-            // ---- P^T fragments (k = token, n = head), f16 high + low parts; with
-            // G <= 4 the low parts ride in the padding columns 4-7 (see emit).
+        for (int off = 4; off <= 16; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+        const float al0 = fast_exp2(st.m[0] - mn0), al1 = fast_exp2(st.m[1] - mn1);
+        st.m[0] = mn0;
+        st.m[1] = mn1;
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t bh[NS][2], bl[NS][2];
+        const bool packed = kQ8 || G <= 4;
+        const bool lo_cols = (lane & 3) >= 2;
+#pragma unroll
+        for (int n = 0; n < NS; ++n) {
+            const float p0 = fast_exp2(x[n][0] - mn0), p1 = fast_exp2(x[n][1] - mn1);
+            const float p2 = fast_exp2(x[n][2] - mn0), p3 = fast_exp2(x[n][3] - mn1);
+            ls0 += p0 + p2;
+            ls1 += p1 + p3;
+            // P^T fragments (k = token, n = head), f16 high + low parts; with G <= 4
+            // the low parts ride in the padding columns 4-7 (see fold).
             uint32_t h01, l01, h23, l23;
             pack_split<kF16>(p0, p1, h01, l01);
             pack_split<kF16>(p2, p3, h23, l23);
-            const bool packed = kQ8 || G <= 4;
-            const bool lo_cols = (lane & 3) >= 2;
-            const uint32_t bh0 = movmatrix_trans(packed && lo_cols ? l01 : h01);
-            const uint32_t bh1 = movmatrix_trans(packed && lo_cols ? l23 : h23);
-            uint32_t bl0 = 0u, bl1 = 0u;
+            bh[n][0] = movmatrix_trans(packed && lo_cols ? l01 : h01);
+            bh[n][1] = movmatrix_trans(packed && lo_cols ? l23 : h23);
+            bl[n][0] = bl[n][1] = 0u;
             if (!packed) {
-                bl0 = movmatrix_trans(l01);
-                bl1 = movmatrix_trans(l23);
+                bl[n][0] = movmatrix_trans(l01);
+                bl[n][1] = movmatrix_trans(l23);
             }
-            // ---- O^T += V^T . P^T
+        }
+        st.l[0] = st.l[0] * al0 + ls0;
+        st.l[1] = st.l[1] * al1 + ls1;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-            for (int mp = 0; mp < KS / 2; ++mp) {
+            for (int mi = 0; mi < KS; ++mi) {
+                st.o[mi][0] *= al0;
+                st.o[mi][1] *= al1;
+                st.o[mi][2] *= al0;
+                st.o[mi][3] *= al1;
+            }
+        }
+        // ---- O^T += V^T . P^T
+#pragma unroll
+        for (int mp = 0; mp < KS / 2; ++mp) {
+#pragma unroll
+            for (int n = 0; n < NS; ++n) {
                 uint32_t r[4];
-                ldsm_x4_trans(r, vb + row * 128u + ((((2u * mp) | csel) ^ sw) << 4));
+                ldsm_x4_trans(r, vb[n] + rofs + ((((2u * mp) | csel) ^ sw) << 4));
                 // r[k] bytes: (tok 2c, dim 2g), (tok 2c, dim 2g+1), (tok 2c+1, dim 2g), (tok 2c+1, dim 2g+1);
                 // r[2hf] holds tokens 0-7 and r[2hf+1] tokens 8-15 of chunk 2mp + hf.
 #pragma unroll
@@ -273,12 +285,55 @@ struct MmaFp8Policy {
                     af[1] = e4m3x2_to_half2(static_cast<uint16_t>(lo >> 16));  // dim 2g+1, tokens 2c, 2c+1
                     af[2] = e4m3x2_to_half2(static_cast<uint16_t>(hi));        // dim 2g,   tokens 8+2c, 9+2c
                     af[3] = e4m3x2_to_half2(static_cast<uint16_t>(hi >> 16));  // dim 2g+1, tokens 8+2c, 9+2c
-                    mma16816<kF16>(st.o[2 * mp + hf], af, bh0, bh1);
-                    if (!packed) mma16816<kF16>(st.o[2 * mp + hf], af, bl0, bl1);
+                    mma16816<kF16>(st.o[2 * mp + hf], af, bh[n][0], bh[n][1]);
+                    if (!packed) mma16816<kF16>(st.o[2 * mp + hf], af, bl[n][0], bl[n][1]);
                 }
             }
         }
+    }
+
+    // One head's part of a stage: kt/vt point at the stage's K/V codes,
+    // [Hc*bs rows][128 B]; this warp's head owns rows hw*bs .. hw*bs+bs-1,
+    // taken two 16-token slices at a time.
+    __device__ __forceinline__ void tile(State& st, const DecodeArgs& a, uint8_t* kt, uint8_t* vt,
+                                         int hw, int n_valid, int G, float*) {
+        const int bs = a.block_size;
+        uint8_t* kh = kt + hw * bs * 128;
+        uint8_t* vh = vt + hw * bs * 128;
+        if (n_valid < bs) zero_tail(vh, n_valid, bs);
+        const uint32_t kb = smem_addr(kh), vb = smem_addr(vh);
+        int mt = 0;
+        for (; mt + 2 <= bs / 16; mt += 2) {
+            const uint32_t k2[2] = {kb + mt * 2048u, kb + (mt + 1) * 2048u};
+            const uint32_t v2[2] = {vb + mt * 2048u, vb + (mt + 1) * 2048u};
+            const int n2[2] = {n_valid - 16 * mt, n_valid - 16 * (mt + 1)};
+            slices<2>(st, a, k2, v2, n2, G);
+        }
+        if (mt < bs / 16) {
+            const uint32_t k1[1] = {kb + mt * 2048u};
+            const uint32_t v1[1] = {vb + mt * 2048u};
+            const int n1[1] = {n_valid - 16 * mt};
+            slices<1>(st, a, k1, v1, n1, G);
+        }
         if (n_valid < bs) fence_proxy_async_smem();  // generic writes before the next TMA fill
+    }
+
+    // Two 16-token blocks (block_size 16) from two stages of one (sequence,
+    // head) run, processed together.
+    static constexpr bool kPairs = true;
+    __device__ __forceinline__ void tile2(State& st, const DecodeArgs& a, uint8_t* kt0, uint8_t* vt0,
+                                          int n0, uint8_t* kt1, uint8_t* vt1, int n1, int hw, int G) {
+        uint8_t* kh0 = kt0 + hw * 16 * 128;
+        uint8_t* vh0 = vt0 + hw * 16 * 128;
+        uint8_t* kh1 = kt1 + hw * 16 * 128;
+        uint8_t* vh1 = vt1 + hw * 16 * 128;
+        if (n0 < 16) zero_tail(vh0, n0, 16);
+        if (n1 < 16) zero_tail(vh1, n1, 16);
+        const uint32_t k2[2] = {smem_addr(kh0), smem_addr(kh1)};
+        const uint32_t v2[2] = {smem_addr(vh0), smem_addr(vh1)};
+        const int n2[2] = {n0, n1};
+        slices<2>(st, a, k2, v2, n2, G);
+        if (n0 < 16 || n1 < 16) fence_proxy_async_smem();
     }
 
     // 16-byte chunk q of row r of head hw's tile (chunk c of a row lands at c ^ (row % 8)).

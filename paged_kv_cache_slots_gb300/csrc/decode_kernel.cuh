@@ -419,7 +419,7 @@ __device__ __forceinline__ bool append_row(const DecodeArgs& a, const Policy& po
 
 // ---------------------------------------------------------------- the kernel
 // Policy provides: State, begin(), tile(), write_state(), write_partial(),
-// write_final(), kTensor, kScratch.
+// write_final(), kTensor, kScratch, kPairs (and tile2() when kPairs).
 template <class Policy>
 __global__ void __launch_bounds__(32 * 16, 1)
     paged_decode_partial_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -520,22 +520,55 @@ __global__ void __launch_bounds__(32 * 16, 1)
         // t % stages, phase (t / stages) & 1); advanced by R per item below.
         int stage = (first - start) % a.stages;
         uint32_t phase = static_cast<uint32_t>((first - start) / a.stages) & 1u;
-        for (int i = first; i < seg_end; i += R) {
-            const bool ok = mbar_wait_bounded(&full[stage], phase, abort, a.status);
+        for (int i = first; i < seg_end;) {
+            // With a policy that takes two 16-token blocks at once, this warp
+            // takes items i and i + R together when both belong to the run.
+            // Waiting for the second while holding the first needs the
+            // producer to have refilled stage (i + R) % stages, i.e. item
+            // i + R - stages to be released: true when stages >= 2R.
+            bool two = false;
+            if constexpr (Policy::kPairs)
+                two = a.block_size == 16 && i + R < seg_end && a.stages >= 2 * R;
+            int stage2 = stage + R;  // R divides the ring size, so this wraps exactly at the end
+            uint32_t phase2 = phase;
+            if (stage2 >= a.stages) {
+                stage2 -= a.stages;
+                phase2 ^= 1u;
+            }
+            bool ok = mbar_wait_bounded(&full[stage], phase, abort, a.status);
+            if (ok && two) ok = mbar_wait_bounded(&full[stage2], phase2, abort, a.status);
             if (ok) {
                 const int j = i - pair_a;
                 const int n_valid = min(a.block_size, ctx - j * a.block_size);
                 uint8_t* kt = ring + stage * 2 * half_bytes;
-                const bool patched = a.k_new && j == nb - 1 && append_row(a, pol, kt, kt + half_bytes, s, h, hw, j, n_valid - 1);
-                pol.tile(st, a, kt, kt + half_bytes, hw, n_valid, G, scratch);
+                bool patched = a.k_new && j == nb - 1 && append_row(a, pol, kt, kt + half_bytes, s, h, hw, j, n_valid - 1);
+                if constexpr (Policy::kPairs) {
+                    if (two) {
+                        const int j1 = j + R;
+                        const int n1 = min(a.block_size, ctx - j1 * a.block_size);
+                        uint8_t* kt1 = ring + stage2 * 2 * half_bytes;
+                        if (a.k_new && j1 == nb - 1)
+                            patched |= append_row(a, pol, kt1, kt1 + half_bytes, s, h, hw, j1, n1 - 1);
+                        pol.tile2(st, a, kt, kt + half_bytes, n_valid, kt1, kt1 + half_bytes, n1, hw, G);
+                    }
+                }
+                if (!two) pol.tile(st, a, kt, kt + half_bytes, hw, n_valid, G, scratch);
                 if (patched) fence_proxy_async_smem();  // generic writes before the next TMA fill
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            stage += R;  // R divides the ring size, so this wraps exactly at the end
-            if (stage >= a.stages) {
-                stage -= a.stages;
-                phase ^= 1u;
+            if (lane == 0) {
+                mbar_arrive(&empty[stage]);
+                if (two) mbar_arrive(&empty[stage2]);
+            }
+            i += two ? 2 * R : R;
+            stage = stage2;
+            phase = phase2;
+            if (two) {
+                stage += R;
+                if (stage >= a.stages) {
+                    stage -= a.stages;
+                    phase ^= 1u;
+                }
             }
         }
         const bool whole = (pair_a >= start) && (pair_b <= end);

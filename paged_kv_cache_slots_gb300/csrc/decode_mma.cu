@@ -25,6 +25,7 @@ template <int DT, int D>
 struct MmaPolicy {
     static constexpr bool kTensor = true;
     static constexpr bool kScratch = false;
+    static constexpr bool kPairs = false;
     static constexpr int KS = D / 16;  // k-steps of QK, m-tiles of PV
     static constexpr int kD = D;
     using T = typename Elem<DT>::T;
