@@ -11,6 +11,12 @@ Functions and the passage each follows (see pkv_oracle.c for the C side):
   paged_decode  -- same Example 3 (history read through the block table) and
                    "Batching and Scheduling", Example 1 (each sequence reads its
                    own KV every step); softmax(scale q.K^T).V in fp64.
+  paged_prefill, slot_mapping_varlen
+                -- multi-token queries (chunked prefill: "Batching and
+                   Scheduling", Example 5; "vLLM Architecture and Installation",
+                   Example 5): new token i of a sequence with context c and n
+                   new tokens sits at position c - n + i and attends causally
+                   to positions 0 .. c - n + i.
   e4m3_encode, quantize_e4m3, append_e4m3, paged_decode(k_scale, v_scale)
                 -- the FP8 KV cache of "vLLM Architecture and Installation",
                    Example 6 (one byte per value): E4M3 codes with one fp32
@@ -77,6 +83,11 @@ def load(path: str | None = None):
         lib.oracle_append_e4m3.argtypes = [c_i, c_i, c_i, c_i, c_i, c_p, c_p, c_i, c_p, c_p, c_p,
                                            ctypes.c_float, ctypes.c_float]
         lib.oracle_append_e4m3.restype = c_i
+        lib.oracle_paged_prefill.argtypes = [c_i, c_p, c_p, c_p, c_p, c_i, c_p, c_p, c_i, c_i, c_i, c_i,
+                                             c_i, c_i, c_d, c_p, c_i]
+        lib.oracle_paged_prefill.restype = c_i
+        lib.oracle_slot_mapping_varlen.argtypes = [c_p, c_i, c_p, c_p, c_i, c_i, c_p]
+        lib.oracle_slot_mapping_varlen.restype = None
         lib.oracle_num_cores.argtypes = []
         lib.oracle_num_cores.restype = c_i
         if path is None:
@@ -217,6 +228,41 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                  _ptr(c), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(out), nthreads)
     if rc != 0:
         raise ValueError(f"oracle_paged_decode failed ({rc})")
+    return out
+
+
+def slot_mapping_varlen(block_tables, query_start, context_lens, block_size: int, lib=None) -> np.ndarray:
+    """Slot of every new token of a multi-token step ([T] int32)."""
+    lib = lib or load()
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    c = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.empty(int(qs[-1]), dtype=np.int32)
+    lib.oracle_slot_mapping_varlen(_ptr(t), t.shape[1], _ptr(qs), _ptr(c), len(c), block_size, _ptr(out))
+    return out
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, scale: float,
+                  nthreads: int = 0, lib=None) -> np.ndarray:
+    """fp64 output [T, Hq, D] of multi-token (causal) queries over the paged cache."""
+    lib = lib or load()
+    dt = _dtype_name(k_cache)
+    if _dtype_name(q) != dt:
+        raise ValueError("q and the cache must share a dtype")
+    qa, kc, vc = _raw(q), _raw(k_cache), _raw(v_cache)
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    c = np.ascontiguousarray(context_lens, dtype=np.int32)
+    T, Hq, D = qa.shape
+    NB, Hkv, bs, D2 = kc.shape
+    B = len(c)
+    assert D == D2 and t.shape[0] == B and len(qs) == B + 1 and int(qs[-1]) == T
+    out = np.empty((T, Hq, D), dtype=np.float64)
+    rc = lib.oracle_paged_prefill(DTYPE_CODE[dt], _ptr(qa), _ptr(kc), _ptr(vc), _ptr(t), t.shape[1],
+                                  _ptr(qs), _ptr(c), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(out),
+                                  nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_paged_prefill failed ({rc})")
     return out
 
 

@@ -305,6 +305,122 @@ int oracle_paged_decode_scaled(int q_dtype, int kv_dtype, double k_scale, double
     return status;
 }
 
+/* Multi-token queries (chunked prefill; "Batching and Scheduling", Example 5,
+ * and "vLLM Architecture and Installation", Example 5: a step gives each
+ * request a number of new tokens, one for a decoding request, a chunk of the
+ * prompt for a prefilling one).  Sequence s brings n_s = query_start[s+1] -
+ * query_start[s] new tokens, already appended, so its cache holds
+ * context_lens[s] tokens and its new tokens sit at positions
+ * context_lens[s] - n_s .. context_lens[s] - 1.  Query token i of s (row
+ * query_start[s] + i of q and out, [T][Hq][D]) attends to the cached tokens at
+ * positions 0 .. context_lens[s] - n_s + i: softmax(scale q.K^T).V over that
+ * causal prefix, read through the block table, fp64. */
+typedef struct {
+    int dtype;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *tables, *qstart, *ctx;
+    int max_blocks, num_seqs, hq, hkv, d, bs, num_blocks;
+    double scale;
+    double* out;
+    int64_t first, last; /* rows (token, head) handled by this worker */
+    int status;
+} orc_pjob;
+
+static void* orc_prefill_rows(void* arg) {
+    orc_pjob* J = (orc_pjob*)arg;
+    int G = J->hq / J->hkv, D = J->d;
+    int64_t cap = 0;
+    double *x = NULL, *qd = (double*)malloc(sizeof(double) * (size_t)D);
+    for (int64_t r = J->first; r < J->last; ++r) {
+        int64_t tok = r / J->hq;
+        int g = (int)(r % J->hq), h = g / G;
+        int s = 0;
+        while (s + 1 < J->num_seqs && J->qstart[s + 1] <= tok) ++s; /* sequence of this token */
+        int n = J->qstart[s + 1] - J->qstart[s];
+        int i = (int)(tok - J->qstart[s]);
+        int last = J->ctx[s] - n + i; /* position of this query token */
+        double* o = J->out + r * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (last < 0) { J->status = -1; continue; }
+        if (last + 1 > cap) {
+            cap = last + 1;
+            x = (double*)realloc(x, sizeof(double) * (size_t)cap);
+        }
+        for (int d = 0; d < D; ++d) qd[d] = orc_load(J->q, (size_t)r * D + d, J->dtype);
+        double mx = -INFINITY;
+        for (int t = 0; t <= last; ++t) { /* scores over the causal prefix */
+            int64_t blk = J->tables[(int64_t)s * J->max_blocks + t / J->bs];
+            if (blk < 0 || blk >= J->num_blocks) { J->status = -1; blk = 0; }
+            size_t base = (size_t)(((blk * J->hkv + h) * J->bs + t % J->bs)) * D;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qd[d] * orc_load(J->k_cache, base + d, J->dtype);
+            x[t] = J->scale * acc;
+            if (x[t] > mx) mx = x[t];
+        }
+        double sum = 0.0;
+        for (int t = 0; t <= last; ++t) {
+            x[t] = exp(x[t] - mx);
+            sum += x[t];
+        }
+        for (int t = 0; t <= last; ++t) {
+            int64_t blk = J->tables[(int64_t)s * J->max_blocks + t / J->bs];
+            if (blk < 0 || blk >= J->num_blocks) blk = 0;
+            size_t base = (size_t)(((blk * J->hkv + h) * J->bs + t % J->bs)) * D;
+            double w = x[t] / sum;
+            for (int d = 0; d < D; ++d) o[d] += w * orc_load(J->v_cache, base + d, J->dtype);
+        }
+    }
+    free(x);
+    free(qd);
+    return NULL;
+}
+
+/* out[T][Hq][D] (fp64) of the multi-token queries described above.  Returns
+ * 0, -1 for a table entry outside the pool or a chunk longer than its context,
+ * -2 for bad head counts. */
+int oracle_paged_prefill(int dtype, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, double scale, double* out,
+                         int nthreads) {
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return -2;
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    int64_t rows = (int64_t)(num_seqs > 0 ? query_start[num_seqs] : 0) * num_q_heads;
+    if (nthreads > rows) nthreads = rows > 0 ? (int)rows : 1;
+    orc_pjob* jobs = (orc_pjob*)calloc((size_t)nthreads, sizeof(orc_pjob));
+    pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    for (int i = 0; i < nthreads; ++i) {
+        orc_pjob j = {dtype, q, k_cache, v_cache, block_tables, query_start, context_lens, max_blocks,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                      rows * i / nthreads, rows * (i + 1) / nthreads, 0};
+        jobs[i] = j;
+    }
+    for (int i = 1; i < nthreads; ++i) pthread_create(&th[i], NULL, orc_prefill_rows, &jobs[i]);
+    orc_prefill_rows(&jobs[0]);
+    int status = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (i) pthread_join(th[i], NULL);
+        if (jobs[i].status) status = jobs[i].status;
+    }
+    free(jobs);
+    free(th);
+    return status;
+}
+
+/* Slot of every new token: token i of sequence s sits at position
+ * context_lens[s] - n_s + i. */
+void oracle_slot_mapping_varlen(const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                                const int32_t* context_lens, int num_seqs, int block_size,
+                                int32_t* slot_out) {
+    for (int s = 0; s < num_seqs; ++s) {
+        int n = query_start[s + 1] - query_start[s];
+        for (int i = 0; i < n; ++i)
+            slot_out[query_start[s] + i] =
+                (int32_t)oracle_slot(block_tables, max_blocks, s, context_lens[s] - n + i, block_size);
+    }
+}
+
 /* The same with q and the cache in one dtype and no cache scaling. */
 int oracle_paged_decode(int dtype, const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_tables, int max_blocks, const int32_t* context_lens,

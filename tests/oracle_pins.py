@@ -29,6 +29,11 @@ What pins what:
                   fp32 quotient x / scale; untouched slots keep their codes.
   fp8 attention-- equals the brute force over the dequantized cache
                   (scale * value), with different K and V scales.
+  multi-token  -- torch's causal scaled_dot_product_attention for whole
+                  prompts; a brute force over the causal prefix after earlier
+                  context; chunking a prompt changes no row; one new token is
+                  the decode step; the worked slots of Example 3 for new
+                  tokens at several positions.
 """
 from __future__ import annotations
 
@@ -383,7 +388,88 @@ def check_fp8_attention(lib):
     assert np.max(np.abs(got - ref)) < 1e-12, "fp8 attention vs dequantized brute force"
 
 
+# ------------------------------------------------------ multi-token queries
+def _prefill_case(rng, ctx, nq, Hq, Hkv, D, bs, np_dt):
+    """Paged pool plus dense per-sequence arrays for a multi-token step."""
+    q_, Kc, Vc, tables, kp, vp = _case(rng, ctx, Hq, Hkv, D, bs, np_dt)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = rng.standard_normal((int(qs[-1]), Hq, D)).astype(np_dt)
+    return q, qs, Kc, Vc, tables, kp, vp
+
+
+def _run_prefill(lib, q, kp, vp, tables, qs, ctx, scale, threads=0):
+    return oracle.paged_prefill(torch.from_numpy(q), torch.from_numpy(kp), torch.from_numpy(vp), tables, qs,
+                                np.array(ctx, np.int32), scale, nthreads=threads, lib=lib)
+
+
+def check_prefill_vs_torch_sdpa(lib):
+    # Whole prompts (no earlier context): causal attention, which torch's
+    # scaled_dot_product_attention computes directly (fp64, heads expanded).
+    rng = np.random.default_rng(61)
+    ctx = [1, 7, 16, 23]
+    Hq, Hkv, D, bs = 6, 2, 16, 4
+    q, qs, Kc, Vc, tables, kp, vp = _prefill_case(rng, ctx, ctx, Hq, Hkv, D, bs, np.float32)
+    scale = 0.3
+    got = _run_prefill(lib, q, kp, vp, tables, qs, ctx, scale)
+    for s, c in enumerate(ctx):
+        qq = torch.from_numpy(q[qs[s]:qs[s + 1]].astype(np.float64)).permute(1, 0, 2)  # [Hq, n, D]
+        kk = torch.from_numpy(Kc[s].astype(np.float64)).repeat_interleave(Hq // Hkv, dim=0)
+        vv = torch.from_numpy(Vc[s].astype(np.float64)).repeat_interleave(Hq // Hkv, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, is_causal=True, scale=scale)
+        err = np.max(np.abs(got[qs[s]:qs[s + 1]] - ref.permute(1, 0, 2).numpy()))
+        assert err < 1e-12, f"causal SDPA, sequence {s}: {err}"
+
+
+def check_prefill_bruteforce_with_context(lib):
+    # Chunks after earlier context, mixed with single-token decodes.
+    rng = np.random.default_rng(62)
+    ctx = [9, 1, 40, 17, 5]
+    nq = [4, 1, 13, 1, 5]
+    Hq, Hkv, D, bs = 8, 2, 8, 4
+    q, qs, Kc, Vc, tables, kp, vp = _prefill_case(rng, ctx, nq, Hq, Hkv, D, bs, np.float16)
+    scale = 0.5
+    got = _run_prefill(lib, q, kp, vp, tables, qs, ctx, scale)
+    G = Hq // Hkv
+    for s, (c, n) in enumerate(zip(ctx, nq)):
+        for i in range(n):
+            pos = c - n + i
+            for g in range(Hq):
+                k = Kc[s][g // G][:pos + 1].astype(np.float64)
+                v = Vc[s][g // G][:pos + 1].astype(np.float64)
+                w = scipy.special.softmax(scale * (k @ q[qs[s] + i, g].astype(np.float64)))
+                assert np.max(np.abs(got[qs[s] + i, g] - w @ v)) < 1e-12, f"seq {s} token {i} head {g}"
+
+
+def check_prefill_chunking_and_decode(lib):
+    rng = np.random.default_rng(63)
+    ctx = [21]
+    Hq, Hkv, D, bs = 4, 2, 8, 4
+    q, qs, Kc, Vc, tables, kp, vp = _prefill_case(rng, ctx, ctx, Hq, Hkv, D, bs, np.float32)
+    whole = _run_prefill(lib, q, kp, vp, tables, qs, ctx, 0.4)
+    # The same prompt in three chunks (8, 8, 5 tokens) gives the same rows.
+    done = 0
+    for n in (8, 8, 5):
+        part = _run_prefill(lib, q[done:done + n], kp, vp, tables, np.array([0, n], np.int32), [done + n], 0.4)
+        assert np.array_equal(part, whole[done:done + n]), "chunked = whole"
+        done += n
+    # A single new token is the decode step.
+    dec = _run(lib, q[20:21], kp, vp, tables, [21], 0.4)
+    assert np.array_equal(dec, whole[20:21]), "one new token = decode"
+
+
+def check_varlen_slots(lib):
+    # The worked slots of "vLLM Architecture and Installation", Example 3:
+    # A (table [1, 2, 3, 6]) positions 9..12 -> 13, 14, 15, 24; B ([4, 5]) position 7 -> 23.
+    g = golden("block_tables_vllm_example3.json")
+    bs = g["block_size"]
+    tables = np.array([[1, 2, 3, 6], [4, 5, -1, -1]], np.int32)
+    got = oracle.slot_mapping_varlen(tables, np.array([0, 4, 5], np.int32), np.array([13, 8], np.int32), bs,
+                                     lib=lib)
+    assert got.tolist() == [13, 14, 15, 24, 23], got
+
+
 ALL_CHECKS = [check_f16_decoder, check_bf16_decoder, check_f32_decoder, check_worked_slots,
               check_append_roundtrip, check_bruteforce, check_closed_forms,
               check_relabel_and_heads, check_e4m3_decoder, check_e4m3_encoder, check_fp8_append,
-              check_fp8_attention]
+              check_fp8_attention, check_prefill_vs_torch_sdpa, check_prefill_bruteforce_with_context,
+              check_prefill_chunking_and_decode, check_varlen_slots]

@@ -20,7 +20,10 @@ MUTATIONS = [
      "return blk * block_size + pos % block_size + 1;"),
     ("head_map_modulo", "int h = g / G;", "int h = g % J->hkv;"),
     ("in_block_offset", "int64_t off = t % J->bs;", "int64_t off = (t + 1) % J->bs;"),
-    ("table_index", "+ t / J->bs];", "+ t % J->bs];"),
+    ("table_index", "+ t / J->bs];\n            if (blk < 0 || blk >= J->num_blocks) { J->status = -1; blk = 0; }\n            int64_t off",
+     "+ t % J->bs];\n            if (blk < 0 || blk >= J->num_blocks) { J->status = -1; blk = 0; }\n            int64_t off"),
+    ("prefill_table_index", "+ t / J->bs];\n            if (blk < 0 || blk >= J->num_blocks) { J->status = -1; blk = 0; }\n            size_t base",
+     "+ t % J->bs];\n            if (blk < 0 || blk >= J->num_blocks) { J->status = -1; blk = 0; }\n            size_t base"),
     ("score_sign", "x[t] = J->scale * acc;", "x[t] = -J->scale * acc;"),
     ("no_max_subtraction", "x[t] = exp(x[t] - mx);", "x[t] = exp(x[t]);"),
     ("no_normalisation", "double w = x[t] / sum;", "double w = x[t];"),
@@ -44,16 +47,42 @@ MUTATIONS = [
     ("append_v_with_k_scale", "head_dim, v_scale, v_cache + dst);", "head_dim, k_scale, v_cache + dst);"),
     ("attention_k_with_v_scale", "K[(size_t)t * D + d] = J->k_scale *", "K[(size_t)t * D + d] = J->v_scale *"),
     ("attention_v_unscaled", "V[(size_t)t * D + d] = J->v_scale *", "V[(size_t)t * D + d] = 1.0 *"),
+    ("prefill_excludes_own_token", "int last = J->ctx[s] - n + i; /* position", "int last = J->ctx[s] - n + i - 1; /* position"),
+    ("prefill_no_context_offset", "int last = J->ctx[s] - n + i; /* position", "int last = i; /* position"),
+    ("prefill_no_causal_mask", "int last = J->ctx[s] - n + i; /* position", "int last = J->ctx[s] - 1; /* position"),
+    ("prefill_head_modulo", "int g = (int)(r % J->hq), h = g / G;", "int g = (int)(r % J->hq), h = g % J->hkv;"),
+    ("varlen_slot_offset", "context_lens[s] - n + i, block_size);", "context_lens[s] - n + i + 1, block_size);"),
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_is_caught(name, old, new, tmp_path):
+# Anchors that occur in both the decode and the multi-token code: (name, old,
+# new, occurrence), the occurrence counted from the top of the source (the
+# decode function comes first).
+SHARED = [
+    ("score_sign", "x[t] = J->scale * acc;", "x[t] = -J->scale * acc;"),
+    ("no_max_subtraction", "x[t] = exp(x[t] - mx);", "x[t] = exp(x[t]);"),
+    ("no_normalisation", "double w = x[t] / sum;", "double w = x[t];"),
+]
+MUTATIONS = [m for m in MUTATIONS if m[0] not in {x[0] for x in SHARED}]
+MUTATIONS = [m + (0,) for m in MUTATIONS] + [m + (0,) for m in SHARED] + \
+    [("prefill_" + m[0], m[1], m[2], 1) for m in SHARED]
+
+
+def _replace_nth(src, old, new, nth):
+    pos = -1
+    for _ in range(nth + 1):
+        pos = src.index(old, pos + 1)
+    return src[:pos] + new + src[pos + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,nth", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new, nth, tmp_path):
     with open(oracle.SOURCE) as f:
         src = f.read()
-    assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
+    expect = 2 if any(name.endswith(m[0]) for m in SHARED) else 1
+    assert src.count(old) == expect, f"mutation anchor for {name} occurs {src.count(old)} times"
     path = tmp_path / "mutant.c"
-    path.write_text(src.replace(old, new))
+    path.write_text(_replace_nth(src, old, new, nth))
     lib = oracle.load(oracle.build(str(path), str(tmp_path / "libmutant.so"), force=True))
     caught = []
     for check in ALL_CHECKS:
