@@ -297,6 +297,51 @@ kv_status_t paged_decode_attention_static(const void* q, const void* k_cache, co
  * KV_ERR_DEVICE_CHECK. */
 kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out);
 
+/* -------------------------------------------------- multi-token queries */
+
+/* A step in which sequence s brings n_s = query_start[s+1] - query_start[s]
+ * new tokens: one for a decoding request, a chunk of the prompt for a
+ * prefilling one ("Batching and Scheduling", Example 5 and "vLLM Architecture
+ * and Installation", Example 5: a token budget per step and chunked prefill).
+ * context_lens[s] counts every cached token of s including the n_s new ones,
+ * which sit at positions context_lens[s] - n_s .. context_lens[s] - 1.
+ * query_start: device int32[num_seqs + 1], non-decreasing, query_start[0] = 0,
+ * query_start[num_seqs] = num_tokens.
+ *
+ * kv_slot_mapping_varlen: slot of every new token (slot_mapping, device
+ * int32[num_tokens]): token i of s goes to table[s][p / bs] * bs + p % bs,
+ * p = context_lens[s] - n_s + i.  Feed it to kv_append with the new rows.
+ * A position outside the table gives -1 and sets KV_FLAG_BAD_CONTEXT, a bad
+ * table entry -1 and KV_FLAG_BAD_BLOCK_ID. */
+kv_status_t kv_slot_mapping_varlen(const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* query_start, const int32_t* context_lens,
+                                   int num_seqs, int num_tokens, int block_size, int num_blocks,
+                                   int32_t* slot_mapping, void* stream);
+
+/* Bytes of the workspace paged_prefill_attention needs (device, 16-byte
+ * aligned, no initialisation). */
+size_t paged_prefill_workspace_bytes(int num_seqs);
+
+/* Causal attention of the new tokens over the paged cache (after their
+ * append): row t = query_start[s] + i of q and out ([num_tokens][Hq][D])
+ * attends to the cached tokens of s at positions 0 .. context_lens[s] - n_s + i,
+ * softmax(scale q.K^T).V with fp32 accumulation; query head g reads KV head
+ * g / (Hq/Hkv).  dtype f16 or bf16 (q and the cache), head_dim 64 or 128,
+ * block_size a multiple of 16 up to 256, Hq/Hkv in {1, 2, 4, 8}; out_dtype
+ * KV_F32 or dtype.  A sequence with n_s > context_lens[s] (or a length past
+ * its table) is skipped (its rows are not written) and sets
+ * KV_FLAG_BAD_CONTEXT.  One CTA per (16 new tokens, KV head); a decoding
+ * sequence (n_s = 1) is served too, but paged_decode_attention is the faster
+ * call for a batch of those. */
+kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                                    int num_blocks, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* query_start,
+                                    const int32_t* context_lens, int num_seqs, int num_tokens,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, kv_dtype_t dtype, float scale, void* out,
+                                    kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
 /* ------------------------------------------------------- FP8 (E4M3) cache */
 
 /* kv_append into a KV_FP8_E4M3 pool: k and v are [n_tokens][Hkv][D] rows in

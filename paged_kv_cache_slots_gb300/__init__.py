@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "KVError", "KVPool", "BlockAllocator", "PrefixCachePool", "kv_pool_bytes", "slot_mapping", "workspace_bytes",
     "paged_decode_attention", "device_status", "library_path", "load_library", "workspace_init",
-    "make_workspace", "paged_decode_append_attention",
+    "make_workspace", "paged_decode_append_attention", "paged_prefill_attention", "slot_mapping_varlen",
 ]
 
 KV_F32, KV_F16, KV_BF16, KV_FP8_E4M3 = 0, 1, 2, 3
@@ -101,6 +101,10 @@ def _declare(lib):
         "paged_decode_append_attention_fp8": (I, [P, P, P, P, I, P, P, ctypes.c_float, ctypes.c_float,
                                                   I, P, I, P, I, I, I, I, I, ctypes.c_float, P, I, P,
                                                   P, SZ, ctypes.POINTER(_DecodeOptions), P]),
+        "paged_prefill_workspace_bytes": (SZ, [I]),
+        "kv_slot_mapping_varlen": (I, [P, I, P, P, I, I, I, I, P, P]),
+        "paged_prefill_attention": (I, [P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, ctypes.c_float, P, I,
+                                        P, SZ, P]),
         "kv_swap_bytes": (SZ, [P, I]),
         "kv_swap_out": (I, [P, P, I, P, SZ, P]),
         "kv_swap_in": (I, [P, P, I, P, SZ, P]),
@@ -430,6 +434,55 @@ def paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, block_table
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
         DTYPE_CODE[q.dtype], float(scale), _ptr(out), DTYPE_CODE[out_dtype], _ptr(slot_mapping),
         _ptr(workspace), workspace.numel(), ctypes.byref(o), _stream(q, stream)), lib)
+    return out
+
+
+def slot_mapping_varlen(block_tables: torch.Tensor, query_start: torch.Tensor, context_lens: torch.Tensor,
+                        block_size: int, num_blocks: int, num_tokens: int | None = None,
+                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Device slot of every new token of a multi-token step (int32 [num_tokens])."""
+    lib = load_library()
+    B = context_lens.shape[0]
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32 and
+          query_start.dtype == torch.int32, "int32 inputs")
+    _need(query_start.shape[0] == B + 1 and block_tables.shape[0] == B and block_tables.is_contiguous(),
+          "query_start [B + 1], block_tables [B, max_blocks]")
+    if num_tokens is None:
+        num_tokens = int(query_start[-1].item())
+    if out is None:
+        out = torch.empty(max(num_tokens, 1), dtype=torch.int32, device=context_lens.device)[:num_tokens]
+    _check(lib.kv_slot_mapping_varlen(_ptr(block_tables), block_tables.shape[1], _ptr(query_start),
+                                      _ptr(context_lens), B, num_tokens, block_size, num_blocks, _ptr(out),
+                                      _stream(context_lens, stream)), lib)
+    return out
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, query_start, context_lens, scale: float,
+                            out=None, out_dtype=None, workspace=None, stream=None):
+    """Causal attention of a step's new tokens (q [T, Hq, D], rows grouped by
+    sequence as query_start says) over the paged cache they were appended to."""
+    lib = load_library()
+    T, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    B = context_lens.shape[0]
+    _need(D == D2 and tuple(v_cache.shape) == tuple(k_cache.shape), "cache shapes")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and the caches share a dtype")
+    _need(all(t.is_contiguous() for t in (q, k_cache, v_cache, block_tables, query_start, context_lens)),
+          "contiguous inputs")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32 and
+          query_start.dtype == torch.int32, "int32 tables")
+    _need(block_tables.shape[0] == B and query_start.shape[0] == B + 1, "table rows / query_start")
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=out_dtype, device=q.device)
+    _need(out.dtype == out_dtype and tuple(out.shape) == (T, Hq, D) and out.is_contiguous(), "out")
+    if workspace is None:
+        workspace = torch.empty(max(16, int(lib.paged_prefill_workspace_bytes(B))), dtype=torch.uint8,
+                                device=q.device)
+    _check(lib.paged_prefill_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
+        _ptr(query_start), _ptr(context_lens), B, T, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale),
+        _ptr(out), DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(), _stream(q, stream)), lib)
     return out
 
 

@@ -713,6 +713,116 @@ kv_status_t paged_decode_append_attention_fp8(const void* q, const void* k_new, 
                        KV_FP8_E4M3, k_scale, v_scale);
 }
 
+// ------------------------------------------------------ multi-token queries
+size_t paged_prefill_workspace_bytes(int num_seqs) {
+    if (num_seqs < 0) return 0;
+    return align256(static_cast<size_t>(num_seqs + 1) * 4);
+}
+
+kv_status_t kv_slot_mapping_varlen(const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                                   const int32_t* context_lens, int num_seqs, int num_tokens, int block_size,
+                                   int num_blocks, int32_t* slot_mapping, void* stream) {
+    if (num_seqs < 0 || num_tokens < 0 || max_blocks <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(KV_ERR_INVALID_ARG, "kv_slot_mapping_varlen: sizes out of range");
+    if (num_seqs == 0) return KV_OK;
+    if (!block_tables || !query_start || !context_lens || (num_tokens > 0 && !slot_mapping))
+        return fail(KV_ERR_INVALID_ARG, "kv_slot_mapping_varlen: null pointer");
+    uint32_t* status = nullptr;
+    if (kv_status_t st = device_info(nullptr, &status, nullptr, nullptr, nullptr)) return st;
+    PrefillArgs a{};
+    a.block_tables = block_tables;
+    a.query_start = query_start;
+    a.context_lens = context_lens;
+    a.status = status;
+    a.num_blocks = num_blocks;
+    a.max_blocks = max_blocks;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.block_size = block_size;
+    a.pdl = 1;
+    cudaError_t e = launch_slot_mapping_varlen(a, slot_mapping, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "varlen slot mapping launch");
+    return KV_OK;
+}
+
+kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                    const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                                    const int32_t* context_lens, int num_seqs, int num_tokens, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size, kv_dtype_t dtype,
+                                    float scale, void* out, kv_dtype_t out_dtype, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+        max_blocks <= 0)
+        return fail(KV_ERR_INVALID_ARG, "paged_prefill_attention: sizes out of range");
+    if (num_q_heads % num_kv_heads)
+        return fail(KV_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                    num_kv_heads);
+    const int G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(KV_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", G);
+    if (head_dim != 64 && head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+    if (block_size % 16 || block_size < 16 || block_size > 256)
+        return fail(KV_ERR_UNSUPPORTED, "multi-token queries need block_size a multiple of 16 up to 256");
+    if (dtype != KV_F16 && dtype != KV_BF16)
+        return fail(KV_ERR_UNSUPPORTED, "multi-token queries run on f16 or bf16");
+    if (out_dtype != KV_F32 && out_dtype != dtype)
+        return fail(KV_ERR_UNSUPPORTED, "out_dtype must be KV_F32 or the input dtype");
+    if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale is not finite");
+    if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size >= (int64_t{1} << 31))
+        return fail(KV_ERR_UNSUPPORTED, "sizes exceed 32-bit row indices");
+    if (num_seqs == 0 || num_tokens == 0) return KV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !query_start || !context_lens || !out || !workspace)
+        return fail(KV_ERR_INVALID_ARG, "paged_prefill_attention: null pointer");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 16))
+        return fail(KV_ERR_INVALID_ARG, "alignment: caches, q, out and the workspace need 16 bytes");
+    if (workspace_bytes < paged_prefill_workspace_bytes(num_seqs))
+        return fail(KV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes,
+                    paged_prefill_workspace_bytes(num_seqs));
+    int dev = 0, max_smem = 0;
+    uint32_t* status = nullptr;
+    if (kv_status_t st = device_info(&dev, &status, nullptr, &max_smem, nullptr)) return st;
+    const int stage_bytes = 2 * block_size * head_dim * 2;
+    int stages = (max_smem - 1024 - 64) / stage_bytes;
+    if (stages > 4) stages = 4;
+    if (stages < 2) return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages");
+    PrefillArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.query_start = query_start;
+    a.context_lens = context_lens;
+    a.out = out;
+    a.tile_cum = static_cast<int32_t*>(workspace);
+    a.status = status;
+    a.num_blocks = num_blocks;
+    a.max_blocks = max_blocks;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.dtype = dtype;
+    a.out_dtype = out_dtype;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.stages = stages;
+    a.smem_bytes = 1024 + stages * stage_bytes + stages * 16 + 16;
+    const int64_t tiles = (static_cast<int64_t>(num_tokens) + 15) / 16 + num_seqs;
+    if (tiles >= (int64_t{1} << 31)) return fail(KV_ERR_UNSUPPORTED, "too many query tiles");
+    a.grid_tiles = static_cast<int>(tiles);
+    a.pdl = 1;
+    a.device = dev;
+    CUtensorMap tk, tv;
+    const int rows = num_blocks * num_kv_heads * block_size;
+    if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, block_size)) return st;
+    if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, block_size)) return st;
+    cudaError_t e = launch_prefill(a, tk, tv, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return KV_OK;
+}
+
 kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out) {
     DeviceGuard g(device);
     if (!g.ok) return fail(KV_ERR_CUDA, "cannot select device %d", device);

@@ -98,6 +98,25 @@ struct DecodeArgs {
     int device;           // CUDA ordinal the launch targets
 };
 
+// Multi-token (chunked-prefill) attention and its plan.
+struct PrefillArgs {
+    const void* q;               // [T][Hq][D]
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* query_start;  // [B + 1]
+    const int32_t* context_lens; // [B]
+    void* out;                   // [T][Hq][D]
+    int32_t* tile_cum;           // [B + 1] workspace: prefix of 16-token tiles per sequence
+    uint32_t* status;
+    int num_blocks, max_blocks, num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size;
+    int dtype, out_dtype;
+    float scale_log2;
+    int stages, smem_bytes, grid_tiles;
+    int pdl;
+    int device;
+};
+
 // Shared-memory plan of the partial kernel.
 struct DecodePlan {
     int stages;
@@ -111,6 +130,9 @@ bool decode_plan(int kernel, int dtype, int head_dim, int block_size, int group,
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_slot_mapping(const SlotArgs& a, cudaStream_t stream);
 cudaError_t launch_swap(const SwapArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                           cudaStream_t stream);
+cudaError_t launch_slot_mapping_varlen(const PrefillArgs& a, int32_t* slots, cudaStream_t stream);
 cudaError_t launch_decode_ffma(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& tmap_k,
                               const CUtensorMap& tmap_v, cudaStream_t stream);

@@ -1,0 +1,138 @@
+"""GPU parity of multi-token queries (chunked prefill) against the oracle.
+
+Bars: the varlen slot mapping and the append of every new token bit-exact;
+attention max |err| <= 2e-3 against the fp64 oracle with fp32 output, plus
+half an ulp of the output type for f16/bf16 output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_slots_gb300 as pkv
+from gpu_harness import bits, check_output
+from workloads import SPECS, make_placement, new_token_counts, pool_layer_values, small_spec, step_token_values
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _step(spec, nq, out_dtype=torch.float32, check_pool=True):
+    """Slot mapping, append and causal attention of one multi-token step,
+    through the library and through the oracle; every output compared."""
+    pl = make_placement(spec)
+    ctx = pl.context_lens
+    nq = np.asarray(nq, np.int32)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    T = int(qs[-1])
+    k_pre, v_pre = pool_layer_values(spec, pl.num_blocks, 0, "cpu")
+    q, kn, vn = step_token_values(spec, T, 0, "cpu")
+    o_slots = oracle.slot_mapping_varlen(pl.block_tables, qs, ctx, spec.block_size)
+    k_post, v_post = oracle.append(k_pre, v_pre, kn, vn, o_slots)
+    ref = oracle.paged_prefill(q, k_post, v_post, pl.block_tables, qs, ctx, spec.attn_scale)
+
+    pool = pkv.KVPool(1, pl.num_blocks, spec.block_size, spec.num_kv_heads, spec.head_dim, spec.torch_dtype)
+    kc, vc = pool.layer(0)
+    kc.copy_(k_pre)
+    vc.copy_(v_pre)
+    tables = torch.from_numpy(pl.block_tables).cuda()
+    ctx_d = torch.from_numpy(ctx).cuda()
+    qs_d = torch.from_numpy(qs).cuda()
+    slots = pkv.slot_mapping_varlen(tables, qs_d, ctx_d, spec.block_size, pl.num_blocks, num_tokens=T)
+    pool.append(0, kn.cuda(), vn.cuda(), slots)
+    out = torch.full((T, spec.num_q_heads, spec.head_dim), float("nan"), dtype=out_dtype, device="cuda")
+    pkv.paged_prefill_attention(q.cuda(), kc, vc, tables, qs_d, ctx_d, spec.attn_scale, out=out,
+                                out_dtype=out_dtype)
+    assert pkv.device_status() == (0, 0)
+    assert np.array_equal(slots.cpu().numpy(), o_slots), "varlen slot mapping"
+    if check_pool:
+        assert torch.equal(bits(kc.cpu()), bits(k_post)) and torch.equal(bits(vc.cpu()), bits(v_post))
+    return check_output(out, ref, f"{spec.name} prefill {out_dtype}")
+
+
+CTX = (1, 15, 16, 17, 33, 64, 100, 257, 40)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_mixed_step_all_shapes(dtype, head_dim, group):
+    spec = small_spec(f"prefill_{dtype}_{head_dim}_{group}", num_q_heads=2 * group, num_kv_heads=2,
+                      head_dim=head_dim, block_size=16, dtype=dtype, seed=100 + head_dim + group, ctx=CTX)
+    nq = new_token_counts(CTX, seed=group, max_chunk=70)
+    nq[-1] = CTX[-1]  # one whole prompt (no earlier context)
+    _step(spec, nq)
+
+
+@pytest.mark.parametrize("block_size", [32, 64])
+def test_other_block_sizes(block_size):
+    ctx = (1, block_size - 1, block_size + 1, 3 * block_size + 5, 200)
+    spec = small_spec(f"prefill_bs{block_size}", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                      block_size=block_size, dtype="bf16", seed=block_size, ctx=ctx)
+    _step(spec, new_token_counts(ctx, seed=3, max_chunk=150))
+
+
+def test_output_in_input_dtype():
+    spec = small_spec("prefill_out_bf16", num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                      dtype="bf16", seed=7, ctx=(300, 17, 1, 64))
+    _step(spec, [70, 17, 1, 5], out_dtype=torch.bfloat16)
+
+
+def test_long_chunk_after_context():
+    # A 2048-token chunk after 2048 tokens of earlier context, next to decodes:
+    # the shape of a chunked-prefill step of the Llama-3-8B-shaped layer.
+    spec = small_spec("prefill_long", num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                      dtype="bf16", seed=9, ctx=(4096, 700, 33, 4096))
+    _step(spec, [2048, 1, 1, 1])
+
+
+def test_chunked_prompt_equals_one_step():
+    # A 300-token prompt processed in chunks of 128, 128, 44 gives the rows of
+    # the prompt processed at once (same cache contents).
+    spec = small_spec("prefill_chunks", num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
+                      dtype="f16", seed=11, ctx=(300,))
+    pl = make_placement(spec)
+    k_pre, _ = pool_layer_values(spec, pl.num_blocks, 0, "cuda")
+    v_pre = torch.randn_like(k_pre.float()).to(k_pre.dtype)
+    q, _, _ = step_token_values(spec, 300, 0, "cuda")
+    tables = torch.from_numpy(pl.block_tables).cuda()
+    whole = pkv.paged_prefill_attention(q, k_pre, v_pre, tables, torch.tensor([0, 300], dtype=torch.int32,
+                                        device="cuda"), torch.tensor([300], dtype=torch.int32, device="cuda"),
+                                        spec.attn_scale, out_dtype=torch.float32)
+    done = 0
+    for n in (128, 128, 44):
+        part = pkv.paged_prefill_attention(q[done:done + n].contiguous(), k_pre, v_pre, tables,
+                                           torch.tensor([0, n], dtype=torch.int32, device="cuda"),
+                                           torch.tensor([done + n], dtype=torch.int32, device="cuda"),
+                                           spec.attn_scale, out_dtype=torch.float32)
+        assert torch.equal(part, whole[done:done + n]), f"chunk at {done}"
+        done += n
+
+
+def test_bad_lengths_flagged_and_skipped():
+    spec = small_spec("prefill_bad", num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+                      dtype="f16", seed=13, ctx=(20, 5))
+    pl = make_placement(spec)
+    k_pre, v_pre = pool_layer_values(spec, pl.num_blocks, 0, "cuda")
+    q, _, _ = step_token_values(spec, 12, 0, "cuda")
+    tables = torch.from_numpy(pl.block_tables).cuda()
+    qs = torch.tensor([0, 4, 12], dtype=torch.int32, device="cuda")  # second: 8 new tokens > 5 cached
+    ctx = torch.tensor([20, 5], dtype=torch.int32, device="cuda")
+    out = torch.full((12, 4, 64), 7.0, dtype=torch.float32, device="cuda")
+    pkv.paged_prefill_attention(q, k_pre, v_pre, tables, qs, ctx, spec.attn_scale, out=out,
+                                out_dtype=torch.float32)
+    st, flags = pkv.device_status()
+    assert flags & pkv.FLAG_BAD_CONTEXT and st != 0
+    assert torch.all(out[4:] == 7.0)  # the bad sequence's rows are not written
+    assert torch.isfinite(out[:4]).all()
+    with pytest.raises(pkv.KVError):
+        pkv.paged_prefill_attention(q.float(), k_pre.float(), v_pre.float(), tables, qs, ctx, 0.1)

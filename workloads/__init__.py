@@ -306,6 +306,30 @@ def step_layer_values(spec: WorkloadSpec, num_seqs: int, layer: int, device="cpu
     return q, kn, vn
 
 
+def step_token_values(spec: WorkloadSpec, num_tokens: int, layer: int, device="cpu"):
+    """q [T, Hq, D] and the new K, V rows [T, Hkv, D] of a step with T new tokens."""
+    q = _normal((num_tokens, spec.num_q_heads, spec.head_dim), spec.torch_dtype,
+                value_seed(spec, layer, 6), device)
+    kn = _normal((num_tokens, spec.num_kv_heads, spec.head_dim), spec.torch_dtype,
+                 value_seed(spec, layer, 7), device)
+    vn = _normal((num_tokens, spec.num_kv_heads, spec.head_dim), spec.torch_dtype,
+                 value_seed(spec, layer, 8), device)
+    return q, kn, vn
+
+
+def new_token_counts(context_lens, seed: int, max_chunk: int, decode_frac: float = 0.5) -> np.ndarray:
+    """New tokens per sequence in a mixed step: a seeded share of decodes (1
+    token), the others a chunk of 2 .. min(context, max_chunk) tokens (a
+    whole prompt when the chunk reaches the context)."""
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    n = np.ones(len(ctx), dtype=np.int32)
+    for s, c in enumerate(ctx):
+        if c >= 2 and rng.random() >= decode_frac:
+            n[s] = int(rng.integers(2, min(int(c), max_chunk) + 1))
+    return n
+
+
 def small_spec(name="custom", *, num_q_heads=4, num_kv_heads=2, head_dim=64,
                block_size=16, dtype="f32", seed=11, ctx=(1, 15, 16, 17, 33),
                num_blocks=0, scale=0.0, kv_dtype="", kv_scales=(1.0, 1.0)) -> WorkloadSpec:
