@@ -40,8 +40,8 @@ NOMINAL_HBM_GBS = 8000.0
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-KERNEL_SOURCES = ("decode_kernel.cuh", "decode_mma.cu", "decode_ffma.cu", "device_utils.cuh",
-                  "decode_plan.cu")
+KERNEL_SOURCES = ("decode_kernel.cuh", "decode_mma.cu", "decode_ffma.cu", "decode_fp8.cu", "mma_frag.cuh",
+                  "device_utils.cuh", "decode_plan.cu")
 
 
 def parse_args():
@@ -67,6 +67,8 @@ def parse_args():
                    help="measure swap-out/in of KV blocks to page-locked host memory instead")
     p.add_argument("--swap-requests", type=int, default=8,
                    help="requests of 2000 tokens (8B shape) swapped per timed copy")
+    p.add_argument("--prefill", action="store_true",
+                   help="time the multi-token (chunked-prefill) step of --workload chunked_prefill_b32 instead")
     p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -513,6 +515,126 @@ def bench_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------- prefill leg
+def bench_prefill(args, world, rank, local):
+    """A multi-token step (chunked prefill next to decodes): for every layer
+    the varlen slot mapping, the append of every new token and the causal
+    attention of the new tokens over the paged cache, captured in a CUDA graph.
+    value = new tokens per second; the roofline is the attention's causal
+    FLOPs (4 * D * Hq per (query, visible key) pair) against the bf16 tensor
+    peak."""
+    import paged_kv_cache_slots_gb300 as pkv
+    from workloads import step_token_values
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, True)
+    spec = SPECS[args.workload if SPECS[args.workload].new_tokens else "chunked_prefill_b32"]
+    if args.layers:
+        spec = dataclasses.replace(spec, num_layers=args.layers)
+    pl = make_placement(spec)
+    ctx = pl.context_lens
+    nq = np.asarray(spec.new_tokens, np.int32)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    T = int(qs[-1])
+    pool = pkv.KVPool(spec.num_layers, pl.num_blocks, spec.block_size, spec.num_kv_heads, spec.head_dim,
+                      spec.torch_dtype, device=device)
+    layers = [pool.layer(l) for l in range(spec.num_layers)]
+    for l, (kc, vc) in enumerate(layers):
+        fill_pool_layer(spec, l, kc, vc)
+    qkv = [step_token_values(spec, T, l, device) for l in range(spec.num_layers)]
+    tables = torch.from_numpy(pl.block_tables).to(device)
+    ctx_d = torch.from_numpy(ctx).to(device)
+    qs_d = torch.from_numpy(qs).to(device)
+    slots = torch.empty(T, dtype=torch.int32, device=device)
+    out = torch.empty((T, spec.num_q_heads, spec.head_dim), dtype=spec.torch_dtype, device=device)
+    ws = torch.empty(int(pkv.load_library().paged_prefill_workspace_bytes(len(ctx))), dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        pkv.slot_mapping_varlen(tables, qs_d, ctx_d, spec.block_size, pl.num_blocks, num_tokens=T, out=slots)
+        for l, (kc, vc) in enumerate(layers):
+            q, kn, vn = qkv[l]
+            pool.append(l, kn, vn, slots)
+            pkv.paged_prefill_attention(q, kc, vc, tables, qs_d, ctx_d, spec.attn_scale, out=out, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st, flags = pkv.device_status(device)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x} after warm-up")
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream(device))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        graph.replay()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / steps, world, device)
+    # Attention alone, one layer, events on its stream (the dominant kernel).
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    for a, b in ev:
+        a.record()
+        pkv.paged_prefill_attention(qkv[0][0], layers[0][0], layers[0][1], tables, qs_d, ctx_d, spec.attn_scale,
+                                    out=out, workspace=ws)
+        b.record()
+    torch.cuda.synchronize()
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[1:])
+    visible = sum(int(n) * (int(c) - int(n)) + int(n) * (int(n) + 1) // 2 for n, c in zip(nq, ctx))
+    flops_layer = 4.0 * spec.head_dim * spec.num_q_heads * visible
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peaks = json.load(f)
+    peak_tf = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops_layer / (attn_ms * 1e-3) / 1e12
+    kv_layer = int(ctx.sum()) * spec.num_kv_heads * spec.head_dim * 2 * spec.elem_bytes
+    if rank != 0:
+        return
+    line = {
+        "metric": "chunked-prefill step new tokens/s",
+        "value": round(T * world / (ms_step * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": spec.dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V, random block placement)",
+        "config": {"workload": f"{spec.name}: {spec.num_layers} layers, {len(ctx)} sequences, {T} new tokens "
+                               f"({int((nq == 1).sum())} decodes + chunks {sorted(int(n) for n in nq if n > 1)}), "
+                               f"contexts up to {int(ctx.max())}, 32q/8kv heads, D{spec.head_dim}, "
+                               f"block {spec.block_size}, {pl.num_blocks}-block pool",
+                   "timing": "CUDA-graph replay of the whole step, CUDA events on the replay stream",
+                   "l2": "each layer reads %.2f GB of K/V (> 129 MB L2)" % (kv_layer / 1e9)},
+        "attention_ms_per_layer": round(attn_ms, 4),
+        "attention_tflops": round(achieved, 1),
+        "kv_gbs_per_layer": round(kv_layer / (attn_ms * 1e-3) / 1e9, 1),
+        "gpu_launches": steps * (1 + 3 * spec.num_layers),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4), "traffic": None,
+                     "kernel": "paged_prefill_kernel (one layer, eager, CUDA events)",
+                     "algorithmic_flops_per_launch": flops_layer,
+                     "peak_source": "measured bf16_tflops (cuBLAS burst)"},
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------- swap leg
 def bench_swap(args, world, rank, local):
     """Swap-out and swap-in throughput of whole KV blocks (every layer's K and V)
@@ -611,6 +733,9 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
     if args.swap:
         bench_swap(args, world, rank, local)
+        return
+    if args.prefill or SPECS[args.workload].new_tokens:
+        bench_prefill(args, world, rank, local)
         return
     bench_ours(args, world, rank, local)
 

@@ -234,8 +234,10 @@ struct PrefillTile {
     }
 };
 
-template <int DT, int D>
-__global__ void __launch_bounds__(32 * 9) paged_prefill_kernel(const PrefillArgs a,
+// G consumer warps (one per query head of the group) + the producer warp;
+// the register budget leaves room for several CTAs per SM.
+template <int DT, int D, int G>
+__global__ void __launch_bounds__(32 * (1 + G), G <= 4 ? 2 : 1) paged_prefill_kernel(const PrefillArgs a,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
     extern __shared__ uint8_t smem_raw[];
@@ -243,7 +245,6 @@ __global__ void __launch_bounds__(32 * 9) paged_prefill_kernel(const PrefillArgs
     pdl_wait();
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int G = a.num_q_heads / a.num_kv_heads;
     const int h = blockIdx.y;
     const int x = blockIdx.x;
     const int tiles = a.tile_cum[a.num_seqs];
@@ -371,20 +372,31 @@ __global__ void __launch_bounds__(32 * 9) paged_prefill_kernel(const PrefillArgs
     if (!*abort) t.finish(a, tok0, rows, head);
 }
 
-template <int DT, int D>
-cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+template <int DT, int D, int G>
+cudaError_t launch_prefill_g(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t stream) {
     static std::atomic<int> configured[64];
-    auto kern = paged_prefill_kernel<DT, D>;
+    auto kern = paged_prefill_kernel<DT, D, G>;
     const bool cacheable = a.device >= 0 && a.device < 64;
     if (!cacheable || configured[a.device].load() < a.smem_bytes) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.smem_bytes);
         if (e != cudaSuccess) return e;
         if (cacheable) configured[a.device].store(a.smem_bytes);
     }
-    const int G = a.num_q_heads / a.num_kv_heads;
     return launch_kernel(kern, dim3(a.grid_tiles, a.num_kv_heads), dim3(32 * (1 + G)),
                          static_cast<size_t>(a.smem_bytes), stream, a.pdl != 0, a, tmk, tmv);
+}
+
+template <int DT, int D>
+cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                             cudaStream_t stream) {
+    switch (a.num_q_heads / a.num_kv_heads) {
+        case 1: return launch_prefill_g<DT, D, 1>(a, tmk, tmv, stream);
+        case 2: return launch_prefill_g<DT, D, 2>(a, tmk, tmv, stream);
+        case 4: return launch_prefill_g<DT, D, 4>(a, tmk, tmv, stream);
+        case 8: return launch_prefill_g<DT, D, 8>(a, tmk, tmv, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace

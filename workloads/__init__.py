@@ -53,6 +53,9 @@ class WorkloadSpec:
     # values; q and the new rows stay in `dtype`).
     kv_dtype: str = ""
     kv_scales: tuple = (1.0, 1.0)
+    # New tokens per sequence for a multi-token (chunked-prefill) step; empty:
+    # a decode step (one new token each).
+    new_tokens: tuple = ()
 
     @property
     def group_size(self) -> int:
@@ -124,6 +127,14 @@ SPECS = {
         num_kv_heads=8, head_dim=128, block_size=16, dtype="bf16", seed=2,
         ctx_dist="const", ctx_const=4096, pool_rule="twice_used",
         kv_dtype="e4m3", kv_scales=(1.0 / 56.0, 1.0 / 44.0)),
+    # A chunked-prefill step at the token budget the pages list for GPUs with
+    # 160 GiB or more (16,384 tokens): 32 decodes at 4096 tokens of context
+    # and a 16,352-token chunk continuing a prompt after 16,384 cached tokens.
+    "chunked_prefill_b32": WorkloadSpec(
+        name="chunked_prefill_b32", num_layers=32, num_seqs=33, num_q_heads=32,
+        num_kv_heads=8, head_dim=128, block_size=16, dtype="bf16", seed=5,
+        ctx_dist="list", ctx_list=(4096,) * 32 + (32736,), pool_rule="twice_used",
+        new_tokens=(1,) * 32 + (16352,)),
     # The serving mix with an FP8 cache (same lengths and placement rule).
     "serving_b256_fp8": WorkloadSpec(
         name="serving_b256_fp8", num_layers=32, num_seqs=256, num_q_heads=32,
