@@ -19,7 +19,7 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIBRARY = os.path.join(LIB_DIR, "libpkv.so")
 SOURCES = ["append.cu", "decode_plan.cu", "decode_ffma.cu", "decode_mma.cu", "decode_fp8.cu",
            "decode_static.cu",
-           "prefix_pool.cpp", "swap.cu", "prefill.cu",
+           "prefix_pool.cpp", "swap.cu", "prefill.cu", "prefill_tc.cu",
            "pkv_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

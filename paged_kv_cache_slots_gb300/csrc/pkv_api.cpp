@@ -782,10 +782,13 @@ kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const vo
     int dev = 0, max_smem = 0;
     uint32_t* status = nullptr;
     if (kv_status_t st = device_info(&dev, &status, nullptr, &max_smem, nullptr)) return st;
+    // The tcgen05 kernel: head_dim 128 and blocks that tile 64-key tiles evenly.
+    const bool tc = head_dim == 128 && (block_size % 64 == 0 || 64 % block_size == 0) &&
+                    prefill_tc_smem_bytes() <= max_smem;
     const int stage_bytes = 2 * block_size * head_dim * 2;
     int stages = (max_smem - 1024 - 64) / stage_bytes;
     if (stages > 4) stages = 4;
-    if (stages < 2) return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages");
+    if (!tc && stages < 2) return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages");
     PrefillArgs a{};
     a.q = q;
     a.k_cache = k_cache;
@@ -808,16 +811,19 @@ kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const vo
     a.out_dtype = out_dtype;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.stages = stages;
-    a.smem_bytes = 1024 + stages * stage_bytes + stages * 16 + 16;
-    const int64_t tiles = (static_cast<int64_t>(num_tokens) + 15) / 16 + num_seqs;
+    a.smem_bytes = tc ? prefill_tc_smem_bytes() : 1024 + stages * stage_bytes + stages * 16 + 16;
+    a.tensor_cores = tc ? 1 : 0;
+    a.tile_tokens = tc ? 128 / G : 16;
+    const int64_t tiles = (static_cast<int64_t>(num_tokens) + a.tile_tokens - 1) / a.tile_tokens + num_seqs;
     if (tiles >= (int64_t{1} << 31)) return fail(KV_ERR_UNSUPPORTED, "too many query tiles");
     a.grid_tiles = static_cast<int>(tiles);
     a.pdl = 1;
     a.device = dev;
     CUtensorMap tk, tv;
     const int rows = num_blocks * num_kv_heads * block_size;
-    if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, block_size)) return st;
-    if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, block_size)) return st;
+    const int box_rows = tc ? (block_size < 64 ? block_size : 64) : block_size;
+    if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, box_rows)) return st;
+    if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, box_rows)) return st;
     cudaError_t e = launch_prefill(a, tk, tv, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return KV_OK;

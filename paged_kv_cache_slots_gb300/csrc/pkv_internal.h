@@ -113,6 +113,8 @@ struct PrefillArgs {
     int dtype, out_dtype;
     float scale_log2;
     int stages, smem_bytes, grid_tiles;
+    int tile_tokens;   // new tokens per CTA (16, or 128 / G on the tcgen05 path)
+    int tensor_cores;  // 1: the tcgen05 kernel (head_dim 128)
     int pdl;
     int device;
 };
@@ -133,6 +135,9 @@ cudaError_t launch_swap(const SwapArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                            cudaStream_t stream);
 cudaError_t launch_slot_mapping_varlen(const PrefillArgs& a, int32_t* slots, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                              cudaStream_t stream);
+int prefill_tc_smem_bytes();
 cudaError_t launch_decode_ffma(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& tmap_k,
                               const CUtensorMap& tmap_v, cudaStream_t stream);

@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kQT = 16;  // new tokens per tile
 
-// cum[s] = sum_{s' < s} ceil(n_s' / 16); cum[B] = tiles.  One block; flags
+// cum[s] = sum_{s' < s} ceil(n_s' / tile_tokens); cum[B] = tiles.  One block; flags
 // a chunk longer than its context or a decreasing query_start.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillArgs a) {
     pdl_allow_next();
@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillArgs a)
             const int n = a.query_start[s + 1] - a.query_start[s];
             const int c = a.context_lens[s];
             if (n < 0 || n > c || c > a.max_blocks * a.block_size) raise_flag(a.status, kFlagBadContext);
-            v = n > 0 && n <= c && c <= a.max_blocks * a.block_size ? (n + kQT - 1) / kQT : 0;
+            v = n > 0 && n <= c && c <= a.max_blocks * a.block_size ? (n + a.tile_tokens - 1) / a.tile_tokens : 0;
         }
         int x = v;
 #pragma unroll
@@ -406,6 +406,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tmk, const C
     if (a.num_seqs == 0 || a.num_tokens == 0) return cudaSuccess;
     cudaError_t e = launch_kernel(prefill_plan_kernel, dim3(1), dim3(1024), 0, stream, a.pdl != 0, a);
     if (e != cudaSuccess) return e;
+    if (a.tensor_cores) return launch_prefill_tc(a, tmk, tmv, stream);
     if (a.dtype == kF16) {
         if (a.head_dim == 64) return launch_prefill_t<kF16, 64>(a, tmk, tmv, stream);
         if (a.head_dim == 128) return launch_prefill_t<kF16, 128>(a, tmk, tmv, stream);

@@ -1,0 +1,365 @@
+// Multi-token queries over the paged cache on the fifth-generation tensor
+// cores (tcgen05): the same operation as prefill.cu ("Batching and
+// Scheduling", Example 5; "vLLM Architecture and Installation", Example 5),
+// for head_dim 128.
+//
+// A CTA takes 128 rows: 128/G new tokens of one sequence times the G query
+// heads that share KV head h (row r = token r / G, head h*G + r % G), and
+// walks the keys 0 .. (its last token's position) in tiles of 64:
+//   warp 4      streams the tile's K and V rows (TMA, 128-byte swizzle) into
+//               a ring of 3 stages;
+//   warp 5      (one lane) issues S = Q . K^T (M 128, N 64, K 128) into one of
+//               two tensor-memory buffers, and O += P . V (M 128, N 128,
+//               K 64) into tensor memory, P as a high and a low half-precision
+//               part from shared memory, V read MN-major from its stage;
+//   warps 0-3   one row each: load the row of S from tensor memory, causal
+//               mask, online softmax (base 2) with a lazy rescale of O (only
+//               when the row's maximum grows by more than 2^8; the exponent
+//               reference stays fixed otherwise, so P <= 256), write P, and
+//               at the end O / l.
+// Every hand-off is an mbarrier with a bounded wait; the ones that recur per
+// tile are doubled per buffer so that a wait can never see a phase two steps
+// old.
+#include "decode_kernel.cuh"
+#include "mma_frag.cuh"
+#include "tc_utils.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kBM = 128;                        // rows per CTA
+constexpr int kNK = 64;                         // keys per key tile
+constexpr int kDim = 128;
+constexpr int kRing = 3;
+constexpr uint32_t kQOff = 0;                   // Q: 2 slices x 128 rows x 128 B
+constexpr uint32_t kRingOff = 2 * kBM * 128;    // 32 KiB
+constexpr uint32_t kHalf = 2 * kNK * 128;       // K (or V) of a key tile: 16 KiB
+constexpr uint32_t kStage = 2 * kHalf;          // 32 KiB
+constexpr uint32_t kPOff = kRingOff + kRing * kStage;  // 128 KiB
+constexpr uint32_t kPHalf = kBM * 128;          // P high (or low) part: 16 KiB
+constexpr uint32_t kPBuf = 2 * kPHalf;          // 32 KiB per buffer
+constexpr uint32_t kBarOff = kPOff + 2 * kPBuf; // 192 KiB
+constexpr uint32_t kTmemCols = 256;             // S buffers (2 x 64) + O (128)
+constexpr float kLazy = 8.f;
+
+struct Bars {
+    uint64_t full[kRing], empty[kRing], s_full[2], s_free[2], p_full[2], pv_done[2];
+    uint32_t tmem;
+    int abort;
+};
+
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+    return mbar_wait_bounded(bar, parity & 1u, abort, status);
+}
+
+template <int DT, int G>
+__global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillArgs a,
+                                                                   const __grid_constant__ CUtensorMap tmk,
+                                                                   const __grid_constant__ CUtensorMap tmv) {
+    using T = typename Elem<DT>::T;
+    constexpr int TPT = kBM / G;  // new tokens per CTA
+    extern __shared__ uint8_t smem_raw[];
+    pdl_allow_next();
+    pdl_wait();
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Bars* B = reinterpret_cast<Bars*>(base + kBarOff);
+    volatile int* abort = &B->abort;
+    const int h = blockIdx.y;
+    const int x = blockIdx.x;
+    if (x >= a.tile_cum[a.num_seqs]) return;
+    const int s = find_sequence(a.tile_cum, a.num_seqs, x);
+    const int qt = x - a.tile_cum[s];
+    const int n = a.query_start[s + 1] - a.query_start[s];
+    const int ctx = a.context_lens[s];
+    const int ntok = min(TPT, n - qt * TPT);
+    const int pos0 = ctx - n + qt * TPT;
+    const int last = pos0 + ntok - 1;
+    const int nkt = last / kNK + 1;
+    const int64_t tok0 = a.query_start[s] + static_cast<int64_t>(qt) * TPT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&B->full[i], 1);
+            mbar_init(&B->empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&B->s_full[i], 1);
+            mbar_init(&B->s_free[i], 4);
+            mbar_init(&B->p_full[i], 4);
+            mbar_init(&B->pv_done[i], 1);
+        }
+        B->abort = 0;
+        fence_barrier_init();
+        prefetch_tensor_map(&tmk);
+        prefetch_tensor_map(&tmv);
+    }
+    if (warp == 0) tc_alloc(&B->tmem, kTmemCols);
+    if (warp < 4) {  // Q rows into shared memory, 128-byte swizzled K-major
+        const int r = tid;
+        const int tr = min(r / G, ntok - 1);
+        const T* qrow = static_cast<const T*>(a.q) + ((tok0 + tr) * a.num_q_heads + h * G + r % G) * kDim;
+#pragma unroll
+        for (int q16 = 0; q16 < 16; ++q16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * q16);
+            *reinterpret_cast<uint4*>(base + kQOff + (q16 >> 3) * (kBM * 128) + r * 128 +
+                                      (((q16 & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = B->tmem;
+
+    if (warp == 4) {
+        // ---- producer: K and V rows of key tiles 0 .. nkt-1 of head h
+        const int bs = a.block_size;
+        const int box = bs < kNK ? bs : kNK;  // rows per TMA box
+        const int nblk = (ctx + bs - 1) / bs;
+        const uint64_t policy = policy_evict_last();
+        int issued = 0;
+        if (lane == 0) {
+            for (int j = 0; j < nkt; ++j) {
+                const int st = j % kRing;
+                if (j >= kRing && !wait(&B->empty[st], j / kRing - 1, abort, a.status)) break;
+                uint8_t* kd = base + kRingOff + st * kStage;
+                uint8_t* vd = kd + kHalf;
+                mbar_arrive_expect_tx(&B->full[st], kStage);
+                for (int b = 0; b < kNK / box; ++b) {
+                    const int key0 = j * kNK + b * box;
+                    const int lb = key0 / bs;
+                    int blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + (lb < nblk ? lb : 0)];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        raise_flag(a.status, kFlagBadBlock);
+                        blk = 0;
+                    }
+                    const int y = (blk * a.num_kv_heads + h) * bs + (key0 - lb * bs);
+                    for (int sl = 0; sl < 2; ++sl) {
+                        tensor_load_2d(kd + sl * (kNK * 128) + b * box * 128, &tmk, sl * 64, y, &B->full[st], policy);
+                        tensor_load_2d(vd + sl * (kNK * 128) + b * box * 128, &tmv, sl * 64, y, &B->full[st], policy);
+                    }
+                }
+                ++issued;
+            }
+            // Every copy issued must land before the CTA can exit.
+            for (int st = 0; st < kRing && st < issued; ++st) {
+                const int lastj = st + ((issued - 1 - st) / kRing) * kRing;
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&B->full[st], (lastj / kRing) & 1)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        raise_flag(a.status, kFlagTimeout);
+                        break;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ---- MMA issue (one lane)
+        if (lane == 0) {
+            constexpr int bf = DT == kBF16 ? 1 : 0;
+            constexpr uint32_t idS = tc_idesc_f16(bf, false, kNK, kBM);
+            constexpr uint32_t idPV = tc_idesc_f16(bf, true, kDim, kBM);
+            const uint32_t qa = smem_addr(base + kQOff);
+            auto pv = [&](int t) -> bool {
+                const int st = t % kRing, bt = t & 1;
+                if (!wait(&B->p_full[bt], t >> 1, abort, a.status)) return false;
+                tc_fence_after();
+                const uint32_t va = smem_addr(base + kRingOff + st * kStage + kHalf);
+                const uint32_t ph = smem_addr(base + kPOff + bt * kPBuf);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kNK / 16; ++kk)
+                        tc_mma(taddr + 128, tc_sdesc(ph + part * kPHalf + kk * 32, 16, 1024),
+                               tc_sdesc(va + kk * 16 * 128, kNK * 128, 1024), idPV,
+                               !(t == 0 && part == 0 && kk == 0));
+                tc_commit(&B->pv_done[bt]);
+                tc_commit(&B->empty[st]);
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < nkt && ok; ++j) {
+                const int st = j % kRing, b = j & 1;
+                ok = wait(&B->full[st], j / kRing, abort, a.status);
+                if (ok && j >= 2) ok = wait(&B->s_free[b], (j >> 1) - 1, abort, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ka = smem_addr(base + kRingOff + st * kStage);
+#pragma unroll
+                for (int ks = 0; ks < kDim / 16; ++ks)
+                    tc_mma(taddr + b * kNK, tc_sdesc(qa + (ks >> 2) * (kBM * 128) + (ks & 3) * 32, 16, 1024),
+                           tc_sdesc(ka + (ks >> 2) * (kNK * 128) + (ks & 3) * 32, 16, 1024), idS, ks > 0);
+                tc_commit(&B->s_full[b]);
+                if (j >= 1) ok = pv(j - 1);
+            }
+            if (ok) pv(nkt - 1);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax: thread r owns row r (tensor-memory lane r)
+        const int r = tid;
+        const int tr = r / G;
+        const int qpos = pos0 + min(tr, ntok - 1);
+        const uint32_t lane_base = taddr + (static_cast<uint32_t>(32 * warp) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt && ok; ++j) {
+            const int b = j & 1;
+            ok = __all_sync(0xffffffffu, wait(&B->s_full[b], j >> 1, abort, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            float sv[kNK];
+            {
+                float t0[32], t1[32];
+                tc_ld32(lane_base + b * kNK, t0);
+                tc_ld32(lane_base + b * kNK + 32, t1);
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    sv[c] = t0[c];
+                    sv[32 + c] = t1[c];
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->s_free[b]);
+            const int kbase = j * kNK;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kNK; ++c) {
+                sv[c] = kbase + c <= qpos ? sv[c] * a.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, sv[c]);
+            }
+            bool need = false;
+            if (j == 0) {
+                m_ref = mt;  // key 0 is visible to every row
+            } else {
+                need = mt > m_ref + kLazy;
+            }
+            if (__any_sync(0xffffffffu, need)) {
+                // O must be complete up to tile j-1 before it is rescaled.
+                ok = __all_sync(0xffffffffu, wait(&B->pv_done[(j - 1) & 1], (j - 1) >> 1, abort, a.status));
+                if (!ok) break;
+                tc_fence_after();
+                const float f = need ? fast_exp2(m_ref - mt) : 1.f;
+                if (need) {
+                    l *= f;
+                    m_ref = mt;
+                }
+#pragma unroll
+                for (int cb = 0; cb < kDim / 32; ++cb) {
+                    float o[32];
+                    tc_ld32(lane_base + 128 + 32 * cb, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] *= f;
+                    tc_st32(lane_base + 128 + 32 * cb, o);
+                }
+                tc_wait_st();
+            }
+            // P buffer b is free once PV of tile j-2 has completed.
+            if (j >= 2) {
+                ok = __all_sync(0xffffffffu, wait(&B->pv_done[b], (j >> 1) - 1, abort, a.status));
+                if (!ok) break;
+            }
+            uint8_t* prow = base + kPOff + b * kPBuf + r * 128;
+            float ps = 0.f;
+#pragma unroll
+            for (int q16 = 0; q16 < kNK / 8; ++q16) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = fast_exp2(sv[8 * q16 + 2 * e] - m_ref);
+                    const float p1 = fast_exp2(sv[8 * q16 + 2 * e + 1] - m_ref);
+                    ps += p0 + p1;
+                    pack_split<DT>(p0, p1, hi[e], lo[e]);
+                }
+                const int sw = ((q16 ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4*>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(prow + kPHalf + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            l += ps;
+            // Keys past the sequence's last token may hold any value in V (even
+            // NaN): zero those rows of the last tile's V so that 0 * V stays 0.
+            if (kbase + kNK > ctx) {
+                const int from = ctx - kbase;
+                uint8_t* vd = base + kRingOff + (j % kRing) * kStage + kHalf;
+                for (int e = r; e < (kNK - from) * 16; e += kBM) {
+                    const int row = from + e / 16, q16 = e % 16;
+                    *reinterpret_cast<uint4*>(vd + (q16 >> 3) * (kNK * 128) + row * 128 +
+                                              (((q16 & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->p_full[b]);  // one arrival per warp (count 4)
+        }
+        if (__all_sync(0xffffffffu, ok && !*abort)) {
+            ok = __all_sync(0xffffffffu, wait(&B->pv_done[(nkt - 1) & 1], (nkt - 1) >> 1, abort, a.status));
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const bool row_ok = ok && tr < ntok;
+            const int64_t o0 = ((tok0 + tr) * a.num_q_heads + h * G + r % G) * kDim;
+#pragma unroll
+            for (int cb = 0; cb < kDim / 32; ++cb) {
+                float o[32];
+                tc_ld32(lane_base + 128 + 32 * cb, o);
+                tc_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) store_out(a.out, o0 + 32 * cb + c, o[c] * inv, a.out_dtype);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(taddr, kTmemCols);
+    }
+}
+
+template <int DT, int G>
+cudaError_t launch_tc_g(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
+    static std::atomic<int> configured[64];
+    auto kern = paged_prefill_tc_kernel<DT, G>;
+    const bool cacheable = a.device >= 0 && a.device < 64;
+    if (!cacheable || configured[a.device].load() < a.smem_bytes) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.smem_bytes);
+        if (e != cudaSuccess) return e;
+        if (cacheable) configured[a.device].store(a.smem_bytes);
+    }
+    return launch_kernel(kern, dim3(a.grid_tiles, a.num_kv_heads), dim3(192), static_cast<size_t>(a.smem_bytes),
+                         stream, a.pdl != 0, a, tmk, tmv);
+}
+
+template <int DT>
+cudaError_t launch_tc_t(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
+    switch (a.num_q_heads / a.num_kv_heads) {
+        case 1: return launch_tc_g<DT, 1>(a, tmk, tmv, stream);
+        case 2: return launch_tc_g<DT, 2>(a, tmk, tmv, stream);
+        case 4: return launch_tc_g<DT, 4>(a, tmk, tmv, stream);
+        case 8: return launch_tc_g<DT, 8>(a, tmk, tmv, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int prefill_tc_smem_bytes() { return static_cast<int>(kBarOff + sizeof(Bars) + 1024); }
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              cudaStream_t stream) {
+    if (a.head_dim != kDim) return cudaErrorInvalidValue;
+    if (a.dtype == kBF16) return launch_tc_t<kBF16>(a, tmk, tmv, stream);
+    if (a.dtype == kF16) return launch_tc_t<kF16>(a, tmk, tmv, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv
