@@ -69,6 +69,8 @@ def parse_args():
                    help="requests of 2000 tokens (8B shape) swapped per timed copy")
     p.add_argument("--prefill", action="store_true",
                    help="time the multi-token (chunked-prefill) step of --workload chunked_prefill_b32 instead")
+    p.add_argument("--block-size", type=int, default=0,
+                   help="override the workload's tokens per block (prefill leg; 0: the workload's)")
     p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -531,6 +533,8 @@ def bench_prefill(args, world, rank, local):
     spec = SPECS[args.workload if SPECS[args.workload].new_tokens else "chunked_prefill_b32"]
     if args.layers:
         spec = dataclasses.replace(spec, num_layers=args.layers)
+    if args.block_size:
+        spec = dataclasses.replace(spec, block_size=args.block_size)
     pl = make_placement(spec)
     ctx = pl.context_lens
     nq = np.asarray(spec.new_tokens, np.int32)

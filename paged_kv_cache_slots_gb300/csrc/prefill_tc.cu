@@ -53,7 +53,10 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile in
     return mbar_wait_bounded(bar, parity & 1u, abort, status);
 }
 
-template <int DT, int G>
+// kLanes: blocks shorter than a key tile are loaded by the producer warp's
+// lanes with 16-byte cp.async copies (one TMA box per (block, 64-dim slice)
+// would cost 16 boxes per 64-key tile at 16-token blocks); longer blocks by TMA.
+template <int DT, int G, bool kLanes>
 __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillArgs a,
                                                                    const __grid_constant__ CUtensorMap tmk,
                                                                    const __grid_constant__ CUtensorMap tmv) {
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
 
     if (tid == 0) {
         for (int i = 0; i < kRing; ++i) {
-            mbar_init(&B->full[i], 1);
+            mbar_init(&B->full[i], kLanes ? 32 : 1);  // one arrival per producer lane, or the TMA count
             mbar_init(&B->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -121,7 +124,51 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
         const int nblk = (ctx + bs - 1) / bs;
         const uint64_t policy = policy_evict_last();
         int issued = 0;
-        if (lane == 0) {
+        if constexpr (kLanes) {
+            // Blocks of 16 or 32 tokens.  Lane e copies the 16-byte chunk e % 8
+            // of rows e / 8, e / 8 + 4, ... of K and V (both 64-dim slices),
+            // written in the 128-byte swizzled layout the tensor copies produce.
+            const char* kc = static_cast<const char*>(a.k_cache);
+            const char* vc = static_cast<const char*>(a.v_cache);
+            const int lg = bs == 16 ? 4 : 5;
+            const int ch = lane & 7;
+            for (int j = 0; j < nkt; ++j) {
+                const int st = j % kRing;
+                if (j >= kRing && !__all_sync(0xffffffffu, wait(&B->empty[st], j / kRing - 1, abort, a.status))) break;
+                // Lane b < 64 / bs holds the tile's block b.
+                int blk = 0;
+                if (lane < (kNK >> lg)) {
+                    const int lb = ((j * kNK) >> lg) + lane;
+                    blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + (lb < nblk ? lb : 0)];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        raise_flag(a.status, kFlagBadBlock);
+                        blk = 0;
+                    }
+                }
+                const uint32_t kd = smem_addr(base + kRingOff + st * kStage);
+#pragma unroll 4
+                for (int r = 0; r < kNK / 4; ++r) {
+                    const int row = (lane >> 3) + 4 * r;
+                    const int bk = __shfl_sync(0xffffffffu, blk, row >> lg);
+                    const int64_t src = ((static_cast<int64_t>(bk) * a.num_kv_heads + h) * bs + (row & (bs - 1))) *
+                                            (kDim * 2) + ch * 16;
+                    const uint32_t dst = kd + row * 128 + ((ch ^ (row & 7)) << 4);
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + sl * (kNK * 128)),
+                                     "l"(kc + src + sl * 128)
+                                     : "memory");
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + kHalf + sl * (kNK * 128)),
+                                     "l"(vc + src + sl * 128)
+                                     : "memory");
+                    }
+                }
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&B->full[st]))
+                             : "memory");
+                ++issued;
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+        } else if (lane == 0) {
             for (int j = 0; j < nkt; ++j) {
                 const int st = j % kRing;
                 if (j >= kRing && !wait(&B->empty[st], j / kRing - 1, abort, a.status)) break;
@@ -187,6 +234,7 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
                 ok = wait(&B->full[st], j / kRing, abort, a.status);
                 if (ok && j >= 2) ok = wait(&B->s_free[b], (j >> 1) - 1, abort, a.status);
                 if (!ok) break;
+                if constexpr (kLanes) fence_proxy_async_smem();  // lane copies before the tensor cores read them
                 tc_fence_after();
                 const uint32_t ka = smem_addr(base + kRingOff + st * kStage);
 #pragma unroll
@@ -325,10 +373,10 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
     }
 }
 
-template <int DT, int G>
-cudaError_t launch_tc_g(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
+template <int DT, int G, bool kLanes>
+cudaError_t launch_tc_l(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
     static std::atomic<int> configured[64];
-    auto kern = paged_prefill_tc_kernel<DT, G>;
+    auto kern = paged_prefill_tc_kernel<DT, G, kLanes>;
     const bool cacheable = a.device >= 0 && a.device < 64;
     if (!cacheable || configured[a.device].load() < a.smem_bytes) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.smem_bytes);
@@ -337,6 +385,12 @@ cudaError_t launch_tc_g(const PrefillArgs& a, const CUtensorMap& tmk, const CUte
     }
     return launch_kernel(kern, dim3(a.grid_tiles, a.num_kv_heads), dim3(192), static_cast<size_t>(a.smem_bytes),
                          stream, a.pdl != 0, a, tmk, tmv);
+}
+
+template <int DT, int G>
+cudaError_t launch_tc_g(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
+    return a.block_size < kNK ? launch_tc_l<DT, G, true>(a, tmk, tmv, stream)
+                              : launch_tc_l<DT, G, false>(a, tmk, tmv, stream);
 }
 
 template <int DT>
