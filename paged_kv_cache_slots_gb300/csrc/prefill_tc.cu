@@ -104,9 +104,16 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
         const int r = tid;
         const int tr = min(r / G, ntok - 1);
         const T* qrow = static_cast<const T*>(a.q) + ((tok0 + tr) * a.num_q_heads + h * G + r % G) * kDim;
+        // A negative scale is applied as |scale| to the scores of -q (a sign
+        // flip is exact), so the row maximum is taken on unscaled scores.
+        const uint32_t flip = a.scale_log2 < 0.f ? 0x80008000u : 0u;
 #pragma unroll
         for (int q16 = 0; q16 < 16; ++q16) {
-            const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * q16);
+            uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * q16);
+            v.x ^= flip;
+            v.y ^= flip;
+            v.z ^= flip;
+            v.w ^= flip;
             *reinterpret_cast<uint4*>(base + kQOff + (q16 >> 3) * (kBM * 128) + r * 128 +
                                       (((q16 & 7) ^ (r & 7)) << 4)) = v;
         }
@@ -254,6 +261,9 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
         const int qpos = pos0 + min(tr, ntok - 1);
         const uint32_t lane_base = taddr + (static_cast<uint32_t>(32 * warp) << 16);
         float m_ref = -INFINITY, l = 0.f;
+        // |scale| in log2 units; a zero scale is taken as 1e-30, which leaves
+        // every finite score's exponent at 0 while masked scores stay -inf.
+        const float sc = fmaxf(fabsf(a.scale_log2), 1e-30f);
         bool ok = true;
         for (int j = 0; j < nkt && ok; ++j) {
             const int b = j & 1;
@@ -277,11 +287,17 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
             if (lane == 0) mbar_arrive(&B->s_free[b]);
             const int kbase = j * kNK;
             float mt = -INFINITY;
+            if (kbase + kNK - 1 > pos0) {  // a key of this tile lies past some row's position
 #pragma unroll
-            for (int c = 0; c < kNK; ++c) {
-                sv[c] = kbase + c <= qpos ? sv[c] * a.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sv[c]);
+                for (int c = 0; c < kNK; ++c) {
+                    sv[c] = kbase + c <= qpos ? sv[c] : -INFINITY;
+                    mt = fmaxf(mt, sv[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kNK; ++c) mt = fmaxf(mt, sv[c]);
             }
+            mt *= sc;
             bool need = false;
             if (j == 0) {
                 m_ref = mt;  // key 0 is visible to every row
@@ -321,8 +337,8 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(sv[8 * q16 + 2 * e] - m_ref);
-                    const float p1 = fast_exp2(sv[8 * q16 + 2 * e + 1] - m_ref);
+                    const float p0 = fast_exp2(fmaf(sv[8 * q16 + 2 * e], sc, -m_ref));
+                    const float p1 = fast_exp2(fmaf(sv[8 * q16 + 2 * e + 1], sc, -m_ref));
                     ps += p0 + p1;
                     pack_split<DT>(p0, p1, hi[e], lo[e]);
                 }

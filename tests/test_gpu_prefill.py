@@ -26,9 +26,10 @@ def _cuda():
     torch.cuda.empty_cache()
 
 
-def _step(spec, nq, out_dtype=torch.float32, check_pool=True):
+def _step(spec, nq, out_dtype=torch.float32, check_pool=True, scale=None):
     """Slot mapping, append and causal attention of one multi-token step,
     through the library and through the oracle; every output compared."""
+    scale = spec.attn_scale if scale is None else scale
     pl = make_placement(spec)
     ctx = pl.context_lens
     nq = np.asarray(nq, np.int32)
@@ -38,7 +39,7 @@ def _step(spec, nq, out_dtype=torch.float32, check_pool=True):
     q, kn, vn = step_token_values(spec, T, 0, "cpu")
     o_slots = oracle.slot_mapping_varlen(pl.block_tables, qs, ctx, spec.block_size)
     k_post, v_post = oracle.append(k_pre, v_pre, kn, vn, o_slots)
-    ref = oracle.paged_prefill(q, k_post, v_post, pl.block_tables, qs, ctx, spec.attn_scale)
+    ref = oracle.paged_prefill(q, k_post, v_post, pl.block_tables, qs, ctx, scale)
 
     pool = pkv.KVPool(1, pl.num_blocks, spec.block_size, spec.num_kv_heads, spec.head_dim, spec.torch_dtype)
     kc, vc = pool.layer(0)
@@ -50,7 +51,7 @@ def _step(spec, nq, out_dtype=torch.float32, check_pool=True):
     slots = pkv.slot_mapping_varlen(tables, qs_d, ctx_d, spec.block_size, pl.num_blocks, num_tokens=T)
     pool.append(0, kn.cuda(), vn.cuda(), slots)
     out = torch.full((T, spec.num_q_heads, spec.head_dim), float("nan"), dtype=out_dtype, device="cuda")
-    pkv.paged_prefill_attention(q.cuda(), kc, vc, tables, qs_d, ctx_d, spec.attn_scale, out=out,
+    pkv.paged_prefill_attention(q.cuda(), kc, vc, tables, qs_d, ctx_d, scale, out=out,
                                 out_dtype=out_dtype)
     assert pkv.device_status() == (0, 0)
     assert np.array_equal(slots.cpu().numpy(), o_slots), "varlen slot mapping"
@@ -79,6 +80,17 @@ def test_other_block_sizes(block_size):
     spec = small_spec(f"prefill_bs{block_size}", num_q_heads=8, num_kv_heads=2, head_dim=128,
                       block_size=block_size, dtype="bf16", seed=block_size, ctx=ctx)
     _step(spec, new_token_counts(ctx, seed=3, max_chunk=150))
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.3])
+def test_negative_zero_and_large_scale(head_dim, scale):
+    # A negative scale favours the keys least aligned with q; a zero scale
+    # gives the mean of V over each token's visible keys.
+    ctx = (1, 40, 130, 77)
+    spec = small_spec(f"prefill_scale_{head_dim}", num_q_heads=8, num_kv_heads=2, head_dim=head_dim,
+                      block_size=16, dtype="bf16", seed=21, ctx=ctx)
+    _step(spec, [1, 40, 65, 3], scale=scale)
 
 
 def test_output_in_input_dtype():
