@@ -6,17 +6,22 @@
 // A CTA takes 128 rows: 128/G new tokens of one sequence times the G query
 // heads that share KV head h (row r = token r / G, head h*G + r % G), and
 // walks the keys 0 .. (its last token's position) in tiles of 64:
-//   warp 4      streams the tile's K and V rows (TMA, 128-byte swizzle) into
-//               a ring of 3 stages;
+//   warp 4      streams the tile's K rows into a ring of 3 stages and its V
+//               rows into a ring of 2 (128-byte swizzle; TMA boxes for
+//               blocks of 64 tokens or more, per-lane 16-byte copies for
+//               shorter blocks);
 //   warp 5      (one lane) issues S = Q . K^T (M 128, N 64, K 128) into one of
 //               two tensor-memory buffers, and O += P . V (M 128, N 128,
-//               K 64) into tensor memory, P as a high and a low half-precision
-//               part from shared memory, V read MN-major from its stage;
+//               K 64) into tensor memory with P read from tensor memory (a
+//               high and a low half-precision part written over the S buffer
+//               it came from) and V read MN-major from its stage;
 //   warps 0-3   one row each: load the row of S from tensor memory, causal
 //               mask, online softmax (base 2) with a lazy rescale of O (only
 //               when the row's maximum grows by more than 2^8; the exponent
 //               reference stays fixed otherwise, so P <= 256), write P, and
 //               at the end O / l.
+// Shared memory (112 KiB) and tensor memory (256 columns) are sized so that
+// two CTAs share an SM: each SM sub-partition then runs two softmax warps.
 // Every hand-off is an mbarrier with a bounded wait; the ones that recur per
 // tile are doubled per buffer so that a wait can never see a phase two steps
 // old.
@@ -31,20 +36,19 @@ namespace {
 constexpr int kBM = 128;                        // rows per CTA
 constexpr int kNK = 64;                         // keys per key tile
 constexpr int kDim = 128;
-constexpr int kRing = 3;
+constexpr int kKRing = 3;                       // K stages
+constexpr int kVRing = 2;                       // V stages
+constexpr uint32_t kHalf = 2 * kNK * 128;       // K (or V) of a key tile: 2 slices of 64 dims, 16 KiB
 constexpr uint32_t kQOff = 0;                   // Q: 2 slices x 128 rows x 128 B
-constexpr uint32_t kRingOff = 2 * kBM * 128;    // 32 KiB
-constexpr uint32_t kHalf = 2 * kNK * 128;       // K (or V) of a key tile: 16 KiB
-constexpr uint32_t kStage = 2 * kHalf;          // 32 KiB
-constexpr uint32_t kPOff = kRingOff + kRing * kStage;  // 128 KiB
-constexpr uint32_t kPHalf = kBM * 128;          // P high (or low) part: 16 KiB
-constexpr uint32_t kPBuf = 2 * kPHalf;          // 32 KiB per buffer
-constexpr uint32_t kBarOff = kPOff + 2 * kPBuf; // 192 KiB
-constexpr uint32_t kTmemCols = 256;             // S buffers (2 x 64) + O (128)
+constexpr uint32_t kKOff = 2 * kBM * 128;       // 32 KiB
+constexpr uint32_t kVOff = kKOff + kKRing * kHalf;   // 80 KiB
+constexpr uint32_t kBarOff = kVOff + kVRing * kHalf; // 112 KiB
+constexpr uint32_t kTmemCols = 256;             // S / P buffers (2 x 64) + O (128)
 constexpr float kLazy = 8.f;
 
 struct Bars {
-    uint64_t full[kRing], empty[kRing], s_full[2], s_free[2], p_full[2], pv_done[2];
+    uint64_t kfull[kKRing], kempty[kKRing], vfull[kVRing], vempty[kVRing];
+    uint64_t s_full[2], p_full[2], pv_done[2];
     uint32_t tmem;
     int abort;
 };
@@ -53,20 +57,28 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile in
     return mbar_wait_bounded(bar, parity & 1u, abort, status);
 }
 
-// kLanes: blocks shorter than a key tile are loaded by the producer warp's
+// kBS 16 or 32: blocks shorter than a key tile, loaded by the producer warp's
 // lanes with 16-byte cp.async copies (one TMA box per (block, 64-dim slice)
-// would cost 16 boxes per 64-key tile at 16-token blocks); longer blocks by TMA.
-template <int DT, int G, bool kLanes>
-__global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillArgs a,
+// would cost 16 boxes per 64-key tile at 16-token blocks); kBS 0: blocks of a
+// multiple of 64 tokens, loaded by TMA.
+template <int DT, int G, int kBS>
+__global__ void __launch_bounds__(192, 2) paged_prefill_tc_kernel(const PrefillArgs a,
                                                                    const __grid_constant__ CUtensorMap tmk,
                                                                    const __grid_constant__ CUtensorMap tmv) {
     using T = typename Elem<DT>::T;
     constexpr int TPT = kBM / G;  // new tokens per CTA
-    extern __shared__ uint8_t smem_raw[];
+    constexpr bool kLanes = kBS != 0;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     pdl_allow_next();
     pdl_wait();
-    uint8_t* base = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // The swizzled layouts need a 1024-byte aligned base; the launch reserves
+    // no slack for re-alignment (two CTAs per SM), so a misaligned window is
+    // reported rather than overrun.
+    if (smem_addr(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) raise_flag(a.status, kFlagBadPlan);
+        return;
+    }
+    uint8_t* base = smem_raw;
     Bars* B = reinterpret_cast<Bars*>(base + kBarOff);
     volatile int* abort = &B->abort;
     const int h = blockIdx.y;
@@ -84,20 +96,26 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int i = 0; i < kRing; ++i) {
-            mbar_init(&B->full[i], kLanes ? 32 : 1);  // one arrival per producer lane, or the TMA count
-            mbar_init(&B->empty[i], 1);
+        // one arrival per producer lane (cp.async), or the TMA byte count
+        for (int i = 0; i < kKRing; ++i) {
+            mbar_init(&B->kfull[i], kLanes ? 32 : 1);
+            mbar_init(&B->kempty[i], 1);
+        }
+        for (int i = 0; i < kVRing; ++i) {
+            mbar_init(&B->vfull[i], kLanes ? 32 : 1);
+            mbar_init(&B->vempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B->s_full[i], 1);
-            mbar_init(&B->s_free[i], 4);
             mbar_init(&B->p_full[i], 4);
             mbar_init(&B->pv_done[i], 1);
         }
         B->abort = 0;
         fence_barrier_init();
-        prefetch_tensor_map(&tmk);
-        prefetch_tensor_map(&tmv);
+        if constexpr (!kLanes) {
+            prefetch_tensor_map(&tmk);
+            prefetch_tensor_map(&tmv);
+        }
     }
     if (warp == 0) tc_alloc(&B->tmem, kTmemCols);
     if (warp < 4) {  // Q rows into shared memory, 128-byte swizzled K-major
@@ -125,90 +143,107 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
     const uint32_t taddr = B->tmem;
 
     if (warp == 4) {
-        // ---- producer: K and V rows of key tiles 0 .. nkt-1 of head h
+        // ---- producer: K rows of key tile i, then V rows of tile i - 1 (K runs
+        // one tile ahead: S of a tile is issued before its PV).
         const int bs = a.block_size;
-        const int box = bs < kNK ? bs : kNK;  // rows per TMA box
         const int nblk = (ctx + bs - 1) / bs;
-        const uint64_t policy = policy_evict_last();
-        int issued = 0;
-        if constexpr (kLanes) {
-            // Blocks of 16 or 32 tokens.  Lane e copies the 16-byte chunk e % 8
-            // of rows e / 8, e / 8 + 4, ... of K and V (both 64-dim slices),
-            // written in the 128-byte swizzled layout the tensor copies produce.
-            const char* kc = static_cast<const char*>(a.k_cache);
-            const char* vc = static_cast<const char*>(a.v_cache);
-            const int lg = bs == 16 ? 4 : 5;
-            const int ch = lane & 7;
-            for (int j = 0; j < nkt; ++j) {
-                const int st = j % kRing;
-                if (j >= kRing && !__all_sync(0xffffffffu, wait(&B->empty[st], j / kRing - 1, abort, a.status))) break;
-                // Lane b < 64 / bs holds the tile's block b.
-                int blk = 0;
-                if (lane < (kNK >> lg)) {
-                    const int lb = ((j * kNK) >> lg) + lane;
-                    blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + (lb < nblk ? lb : 0)];
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        raise_flag(a.status, kFlagBadBlock);
-                        blk = 0;
-                    }
-                }
-                const uint32_t kd = smem_addr(base + kRingOff + st * kStage);
-#pragma unroll 4
-                for (int r = 0; r < kNK / 4; ++r) {
-                    const int row = (lane >> 3) + 4 * r;
-                    const int bk = __shfl_sync(0xffffffffu, blk, row >> lg);
-                    const int64_t src = ((static_cast<int64_t>(bk) * a.num_kv_heads + h) * bs + (row & (bs - 1))) *
-                                            (kDim * 2) + ch * 16;
-                    const uint32_t dst = kd + row * 128 + ((ch ^ (row & 7)) << 4);
-#pragma unroll
-                    for (int sl = 0; sl < 2; ++sl) {
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + sl * (kNK * 128)),
-                                     "l"(kc + src + sl * 128)
-                                     : "memory");
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + kHalf + sl * (kNK * 128)),
-                                     "l"(vc + src + sl * 128)
-                                     : "memory");
-                    }
-                }
-                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&B->full[st]))
-                             : "memory");
-                ++issued;
+        auto block_of = [&](int lb) -> int {
+            int blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + (lb < nblk ? lb : 0)];
+            if (blk < 0 || blk >= a.num_blocks) {
+                raise_flag(a.status, kFlagBadBlock);
+                blk = 0;
             }
-            asm volatile("cp.async.wait_all;" ::: "memory");
-        } else if (lane == 0) {
-            for (int j = 0; j < nkt; ++j) {
-                const int st = j % kRing;
-                if (j >= kRing && !wait(&B->empty[st], j / kRing - 1, abort, a.status)) break;
-                uint8_t* kd = base + kRingOff + st * kStage;
-                uint8_t* vd = kd + kHalf;
-                mbar_arrive_expect_tx(&B->full[st], kStage);
-                for (int b = 0; b < kNK / box; ++b) {
-                    const int key0 = j * kNK + b * box;
-                    const int lb = key0 / bs;
-                    int blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + (lb < nblk ? lb : 0)];
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        raise_flag(a.status, kFlagBadBlock);
-                        blk = 0;
-                    }
-                    const int y = (blk * a.num_kv_heads + h) * bs + (key0 - lb * bs);
-                    for (int sl = 0; sl < 2; ++sl) {
-                        tensor_load_2d(kd + sl * (kNK * 128) + b * box * 128, &tmk, sl * 64, y, &B->full[st], policy);
-                        tensor_load_2d(vd + sl * (kNK * 128) + b * box * 128, &tmv, sl * 64, y, &B->full[st], policy);
+            return blk;
+        };
+        int kiss = 0, viss = 0;
+        if constexpr (kLanes) {
+            // Blocks of kBS = 16 or 32 tokens.  Lane e copies the 16-byte chunk
+            // e % 8 of the tile's rows e / 8 + 4 q (both 64-dim slices) into the
+            // 128-byte swizzled layout the tensor copies produce; row e / 8 + 4 q
+            // lies in block q / (kBS / 4), so every address is a per-lane base
+            // plus a constant.
+            constexpr int kBlk = kNK / kBS;
+            constexpr int kRows = kBS / 4;  // this lane's rows per block
+            const int ch = lane & 7, l8 = lane >> 3;
+            const int64_t lane_src = l8 * (kDim * 2) + ch * 16;
+            const uint32_t lane_dst = l8 * 128;
+            const uint32_t sw0 = static_cast<uint32_t>(ch ^ l8) << 4, sw1 = static_cast<uint32_t>(ch ^ (l8 + 4)) << 4;
+            auto load = [&](int j, const void* cache, uint32_t dst, uint64_t* bar) {
+                const char* c0 = static_cast<const char*>(cache) + lane_src;
+#pragma unroll
+                for (int bb = 0; bb < kBlk; ++bb) {
+                    const char* src =
+                        c0 + (static_cast<int64_t>(block_of(j * kBlk + bb)) * a.num_kv_heads + h) * (kBS * kDim * 2);
+#pragma unroll
+                    for (int q = 0; q < kRows; ++q) {
+                        const int r = bb * kRows + q;
+                        const uint32_t d = dst + lane_dst + r * 512 + ((r & 1) ? sw1 : sw0);
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src + q * 1024)
+                                     : "memory");
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + kNK * 128),
+                                     "l"(src + q * 1024 + 128)
+                                     : "memory");
                     }
                 }
-                ++issued;
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+            };
+            for (int i = 0; i <= nkt; ++i) {
+                if (i < nkt) {
+                    if (i >= kKRing &&
+                        !__all_sync(0xffffffffu, wait(&B->kempty[i % kKRing], i / kKRing - 1, abort, a.status)))
+                        break;
+                    load(i, a.k_cache, smem_addr(base + kKOff + (i % kKRing) * kHalf), &B->kfull[i % kKRing]);
+                    ++kiss;
+                }
+                if (i >= 1) {
+                    const int j = i - 1;
+                    if (j >= kVRing &&
+                        !__all_sync(0xffffffffu, wait(&B->vempty[j % kVRing], j / kVRing - 1, abort, a.status)))
+                        break;
+                    load(j, a.v_cache, smem_addr(base + kVOff + (j % kVRing) * kHalf), &B->vfull[j % kVRing]);
+                    ++viss;
+                }
             }
             // Every copy issued must land before the CTA can exit.
-            for (int st = 0; st < kRing && st < issued; ++st) {
-                const int lastj = st + ((issued - 1 - st) / kRing) * kRing;
-                const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(&B->full[st], (lastj / kRing) & 1)) {
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
-                        raise_flag(a.status, kFlagTimeout);
-                        break;
-                    }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+        } else if (lane == 0) {
+            const uint64_t policy = policy_evict_last();
+            auto load = [&](int j, const CUtensorMap* map, uint8_t* dst, uint64_t* bar) {
+                // Blocks of a multiple of 64 tokens: one block holds the whole tile.
+                mbar_arrive_expect_tx(bar, kHalf);
+                const int key0 = j * kNK;
+                const int lb = key0 / bs;
+                const int y = (block_of(lb) * a.num_kv_heads + h) * bs + (key0 - lb * bs);
+                for (int sl = 0; sl < 2; ++sl) tensor_load_2d(dst + sl * (kNK * 128), map, sl * 64, y, bar, policy);
+            };
+            for (int i = 0; i <= nkt; ++i) {
+                if (i < nkt) {
+                    if (i >= kKRing && !wait(&B->kempty[i % kKRing], i / kKRing - 1, abort, a.status)) break;
+                    load(i, &tmk, base + kKOff + (i % kKRing) * kHalf, &B->kfull[i % kKRing]);
+                    ++kiss;
+                }
+                if (i >= 1) {
+                    const int j = i - 1;
+                    if (j >= kVRing && !wait(&B->vempty[j % kVRing], j / kVRing - 1, abort, a.status)) break;
+                    load(j, &tmv, base + kVOff + (j % kVRing) * kHalf, &B->vfull[j % kVRing]);
+                    ++viss;
                 }
             }
+            // Every copy issued must land before the CTA can exit.
+            auto drain = [&](uint64_t* bars, int ring, int issued) {
+                for (int st = 0; st < ring && st < issued; ++st) {
+                    const int lastj = st + ((issued - 1 - st) / ring) * ring;
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(&bars[st], (lastj / ring) & 1)) {
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            raise_flag(a.status, kFlagTimeout);
+                            break;
+                        }
+                    }
+                }
+            };
+            drain(B->kfull, kKRing, kiss);
+            drain(B->vfull, kVRing, viss);
         }
         __syncwarp();
     } else if (warp == 5) {
@@ -219,36 +254,39 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
             constexpr uint32_t idPV = tc_idesc_f16(bf, true, kDim, kBM);
             const uint32_t qa = smem_addr(base + kQOff);
             auto pv = [&](int t) -> bool {
-                const int st = t % kRing, bt = t & 1;
+                const int sv = t % kVRing, bt = t & 1;
                 if (!wait(&B->p_full[bt], t >> 1, abort, a.status)) return false;
+                if (!wait(&B->vfull[sv], t / kVRing, abort, a.status)) return false;
+                if constexpr (kLanes) fence_proxy_async_smem();  // lane copies before the tensor cores read them
                 tc_fence_after();
-                const uint32_t va = smem_addr(base + kRingOff + st * kStage + kHalf);
-                const uint32_t ph = smem_addr(base + kPOff + bt * kPBuf);
+                const uint32_t va = smem_addr(base + kVOff + sv * kHalf);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kNK / 16; ++kk)
-                        tc_mma(taddr + 128, tc_sdesc(ph + part * kPHalf + kk * 32, 16, 1024),
-                               tc_sdesc(va + kk * 16 * 128, kNK * 128, 1024), idPV,
-                               !(t == 0 && part == 0 && kk == 0));
+                        tc_mma_ts(taddr + 128, taddr + bt * kNK + part * 32 + kk * 8,
+                                  tc_sdesc(va + kk * 16 * 128, kNK * 128, 1024), idPV,
+                                  !(t == 0 && part == 0 && kk == 0));
                 tc_commit(&B->pv_done[bt]);
-                tc_commit(&B->empty[st]);
+                tc_commit(&B->vempty[sv]);
                 return true;
             };
             bool ok = true;
             for (int j = 0; j < nkt && ok; ++j) {
-                const int st = j % kRing, b = j & 1;
-                ok = wait(&B->full[st], j / kRing, abort, a.status);
-                if (ok && j >= 2) ok = wait(&B->s_free[b], (j >> 1) - 1, abort, a.status);
+                const int sk = j % kKRing, b = j & 1;
+                ok = wait(&B->kfull[sk], j / kKRing, abort, a.status);
+                // S buffer b holds P of tile j - 2 until that PV has completed.
+                if (ok && j >= 2) ok = wait(&B->pv_done[b], (j >> 1) - 1, abort, a.status);
                 if (!ok) break;
-                if constexpr (kLanes) fence_proxy_async_smem();  // lane copies before the tensor cores read them
+                if constexpr (kLanes) fence_proxy_async_smem();
                 tc_fence_after();
-                const uint32_t ka = smem_addr(base + kRingOff + st * kStage);
+                const uint32_t ka = smem_addr(base + kKOff + sk * kHalf);
 #pragma unroll
                 for (int ks = 0; ks < kDim / 16; ++ks)
                     tc_mma(taddr + b * kNK, tc_sdesc(qa + (ks >> 2) * (kBM * 128) + (ks & 3) * 32, 16, 1024),
                            tc_sdesc(ka + (ks >> 2) * (kNK * 128) + (ks & 3) * 32, 16, 1024), idS, ks > 0);
                 tc_commit(&B->s_full[b]);
+                tc_commit(&B->kempty[sk]);
                 if (j >= 1) ok = pv(j - 1);
             }
             if (ok) pv(nkt - 1);
@@ -282,22 +320,20 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
                     sv[32 + c] = t1[c];
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B->s_free[b]);
             const int kbase = j * kNK;
-            float mt = -INFINITY;
             if (kbase + kNK - 1 > pos0) {  // a key of this tile lies past some row's position
 #pragma unroll
-                for (int c = 0; c < kNK; ++c) {
-                    sv[c] = kbase + c <= qpos ? sv[c] : -INFINITY;
-                    mt = fmaxf(mt, sv[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kNK; ++c) mt = fmaxf(mt, sv[c]);
+                for (int c = 0; c < kNK; ++c) sv[c] = kbase + c <= qpos ? sv[c] : -INFINITY;
             }
-            mt *= sc;
+            // Row maximum as eight independent chains (short dependency path).
+            float mx[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx[c] = sv[c];
+#pragma unroll
+            for (int c = 8; c < kNK; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                             sc;
             bool need = false;
             if (j == 0) {
                 m_ref = mt;  // key 0 is visible to every row
@@ -325,40 +361,37 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
                 }
                 tc_wait_st();
             }
-            // P buffer b is free once PV of tile j-2 has completed.
-            if (j >= 2) {
-                ok = __all_sync(0xffffffffu, wait(&B->pv_done[b], (j >> 1) - 1, abort, a.status));
-                if (!ok) break;
-            }
-            uint8_t* prow = base + kPOff + b * kPBuf + r * 128;
-            float ps = 0.f;
+            // P over the S buffer it came from: columns 0-31 the high part,
+            // 32-63 the low part, keys 2c and 2c + 1 in column c.
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int q16 = 0; q16 < kNK / 8; ++q16) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(fmaf(sv[8 * q16 + 2 * e], sc, -m_ref));
-                    const float p1 = fast_exp2(fmaf(sv[8 * q16 + 2 * e + 1], sc, -m_ref));
-                    ps += p0 + p1;
-                    pack_split<DT>(p0, p1, hi[e], lo[e]);
+                for (int c = 0; c < kNK / 2; ++c) {
+                    const float p0 = fast_exp2(fmaf(sv[2 * c], sc, -m_ref));
+                    const float p1 = fast_exp2(fmaf(sv[2 * c + 1], sc, -m_ref));
+                    ps[c & 3] += p0 + p1;
+                    pack_split<DT>(p0, p1, hi[c], lo[c]);
                 }
-                const int sw = ((q16 ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(prow + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(prow + kPHalf + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                tc_st32u(lane_base + b * kNK, hi);
+                tc_st32u(lane_base + b * kNK + 32, lo);
             }
-            l += ps;
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             // Keys past the sequence's last token may hold any value in V (even
             // NaN): zero those rows of the last tile's V so that 0 * V stays 0.
             if (kbase + kNK > ctx) {
+                ok = __all_sync(0xffffffffu, wait(&B->vfull[j % kVRing], j / kVRing, abort, a.status));
+                if (!ok) break;
                 const int from = ctx - kbase;
-                uint8_t* vd = base + kRingOff + (j % kRing) * kStage + kHalf;
+                uint8_t* vd = base + kVOff + (j % kVRing) * kHalf;
                 for (int e = r; e < (kNK - from) * 16; e += kBM) {
                     const int row = from + e / 16, q16 = e % 16;
                     *reinterpret_cast<uint4*>(vd + (q16 >> 3) * (kNK * 128) + row * 128 +
                                               (((q16 & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
+            tc_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B->p_full[b]);  // one arrival per warp (count 4)
@@ -389,10 +422,10 @@ __global__ void __launch_bounds__(192, 1) paged_prefill_tc_kernel(const PrefillA
     }
 }
 
-template <int DT, int G, bool kLanes>
+template <int DT, int G, int kBS>
 cudaError_t launch_tc_l(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
     static std::atomic<int> configured[64];
-    auto kern = paged_prefill_tc_kernel<DT, G, kLanes>;
+    auto kern = paged_prefill_tc_kernel<DT, G, kBS>;
     const bool cacheable = a.device >= 0 && a.device < 64;
     if (!cacheable || configured[a.device].load() < a.smem_bytes) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.smem_bytes);
@@ -405,8 +438,10 @@ cudaError_t launch_tc_l(const PrefillArgs& a, const CUtensorMap& tmk, const CUte
 
 template <int DT, int G>
 cudaError_t launch_tc_g(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
-    return a.block_size < kNK ? launch_tc_l<DT, G, true>(a, tmk, tmv, stream)
-                              : launch_tc_l<DT, G, false>(a, tmk, tmv, stream);
+    if (a.block_size == 16) return launch_tc_l<DT, G, 16>(a, tmk, tmv, stream);
+    if (a.block_size == 32) return launch_tc_l<DT, G, 32>(a, tmk, tmv, stream);
+    if (a.block_size % kNK == 0) return launch_tc_l<DT, G, 0>(a, tmk, tmv, stream);
+    return cudaErrorInvalidValue;
 }
 
 template <int DT>
@@ -422,7 +457,7 @@ cudaError_t launch_tc_t(const PrefillArgs& a, const CUtensorMap& tmk, const CUte
 
 }  // namespace
 
-int prefill_tc_smem_bytes() { return static_cast<int>(kBarOff + sizeof(Bars) + 1024); }
+int prefill_tc_smem_bytes() { return static_cast<int>(kBarOff + sizeof(Bars)); }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                               cudaStream_t stream) {
