@@ -74,7 +74,7 @@ def test_mixed_step_all_shapes(dtype, head_dim, group):
     _step(spec, nq)
 
 
-@pytest.mark.parametrize("block_size", [32, 64])
+@pytest.mark.parametrize("block_size", [32, 64, 128])
 def test_other_block_sizes(block_size):
     ctx = (1, block_size - 1, block_size + 1, 3 * block_size + 5, 200)
     spec = small_spec(f"prefill_bs{block_size}", num_q_heads=8, num_kv_heads=2, head_dim=128,
