@@ -42,6 +42,8 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_mma.cu", "decode_ffma.cu", "decode_fp8.cu", "mma_frag.cuh",
                   "device_utils.cuh", "decode_plan.cu")
+PREFILL_SOURCES = ("prefill_tc.cu", "prefill.cu", "tc_utils.cuh", "decode_kernel.cuh", "mma_frag.cuh",
+                   "device_utils.cuh")
 
 
 def parse_args():
@@ -120,20 +122,20 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_slots_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_name: str, workload: str):
+def recorded_traffic(kernel_name: str, workload: str, sources=KERNEL_SOURCES):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(sources)
     for line in open(path):
         if line.startswith("#") or not line.strip():
             continue
@@ -598,6 +600,11 @@ def bench_prefill(args, world, rank, local):
     torch.cuda.synchronize()
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[1:])
     visible = sum(int(n) * (int(c) - int(n)) + int(n) * (int(n) + 1) // 2 for n, c in zip(nq, ctx))
+    # The library takes the tcgen05 kernel for head_dim 128 and blocks that tile 64 keys.
+    tc = spec.head_dim == 128 and (spec.block_size % 64 == 0 or 64 % spec.block_size == 0)
+    kernel_name = ("paged_prefill_tc_kernel<%s,G%d,bs%d>" % (spec.dtype, spec.num_q_heads // spec.num_kv_heads,
+                                                             spec.block_size)
+                   if tc else "paged_prefill_kernel<%s,%d>" % (spec.dtype, spec.head_dim))
     flops_layer = 4.0 * spec.head_dim * spec.num_q_heads * visible
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         peaks = json.load(f)
@@ -630,8 +637,9 @@ def bench_prefill(args, world, rank, local):
         "kv_gbs_per_layer": round(kv_layer / (attn_ms * 1e-3) / 1e9, 1),
         "gpu_launches": steps * (1 + 3 * spec.num_layers),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_tf, 4), "traffic": None,
-                     "kernel": "paged_prefill_kernel (one layer, eager, CUDA events)",
+                     "frac": round(achieved / peak_tf, 4),
+                     "traffic": recorded_traffic(kernel_name, spec.name, PREFILL_SOURCES),
+                     "kernel": kernel_name + " (one layer, eager, CUDA events)",
                      "algorithmic_flops_per_launch": flops_layer,
                      "peak_source": "measured bf16_tflops (cuBLAS burst)"},
         "clocks": clocks.summary(),
