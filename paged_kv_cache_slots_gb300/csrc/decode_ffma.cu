@@ -70,6 +70,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 template <int DT, int D, int G>
 struct FfmaPolicy {
+    static constexpr int kMaxThreads = 32 * 16;
     static constexpr bool kTensor = false;
     static constexpr bool kScratch = true;
     static constexpr bool kPairs = false;

@@ -42,8 +42,12 @@ namespace pkv {
 // larger than half of it, so it fits 4 bits): columns 0-3 carry hi and
 // columns 4-7 lo of heads col % G, and the two halves of each score are
 // added with one shuffle.  Scores then carry scale * log2(e) * k_scale * 2^-kq.
-template <int QT, int D, bool kQ8 = false>
+// kMaxT: the largest block the instantiation is launched with.  The usual
+// launch (1 + 8 warps) takes the 384-thread variant, whose register budget
+// (168 per thread) holds the state without spilling.
+template <int QT, int D, bool kQ8 = false, int kMaxT = 32 * 16>
 struct MmaFp8Policy {
+    static constexpr int kMaxThreads = kMaxT;
     static_assert(D == 128, "E4M3 rows of 128 codes: one 128-byte slice per row");
     static_assert(!kQ8 || QT == kBF16, "the E4M3 QK path splits a bf16 q exactly");
     static constexpr bool kTensor = true;
@@ -439,7 +443,11 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& tmk, const
     if (a.kv_dtype != kFP8 || a.head_dim != 128) return cudaErrorInvalidValue;
     const int G = a.num_q_heads / a.num_kv_heads;
     if (a.dtype == kF16) return launch_partial<MmaFp8Policy<kF16, 128>>(a, tmk, tmv, stream);
-    if (a.dtype == kBF16 && G <= 4) return launch_partial<MmaFp8Policy<kBF16, 128, true>>(a, tmk, tmv, stream);
+    if (a.dtype == kBF16 && G <= 4) {
+        if (32 * (1 + a.consumer_warps) <= 32 * 12)
+            return launch_partial<MmaFp8Policy<kBF16, 128, true, 32 * 12>>(a, tmk, tmv, stream);
+        return launch_partial<MmaFp8Policy<kBF16, 128, true>>(a, tmk, tmv, stream);
+    }
     if (a.dtype == kBF16) return launch_partial<MmaFp8Policy<kBF16, 128>>(a, tmk, tmv, stream);
     return cudaErrorInvalidValue;
 }

@@ -419,9 +419,10 @@ __device__ __forceinline__ bool append_row(const DecodeArgs& a, const Policy& po
 
 // ---------------------------------------------------------------- the kernel
 // Policy provides: State, begin(), tile(), write_state(), write_partial(),
-// write_final(), kTensor, kScratch, kPairs (and tile2() when kPairs).
+// write_final(), kTensor, kScratch, kPairs (and tile2() when kPairs), and
+// kMaxThreads, the largest block it is launched with (its register budget).
 template <class Policy>
-__global__ void __launch_bounds__(32 * 16, 1)
+__global__ void __launch_bounds__(Policy::kMaxThreads, 1)
     paged_decode_partial_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                                 const __grid_constant__ CUtensorMap tmv) {
     extern __shared__ uint8_t smem_raw[];
@@ -629,6 +630,7 @@ cudaError_t launch_partial(const DecodeArgs& a, const CUtensorMap& tmk, const CU
         if (e != cudaSuccess) return e;
         if (cacheable) configured[a.device].store(a.smem_bytes);
     }
+    if (32 * (1 + a.consumer_warps) > Policy::kMaxThreads) return cudaErrorInvalidValue;
     return launch_kernel(kern, dim3(a.num_ctas), dim3(32 * (1 + a.consumer_warps)),
                          static_cast<size_t>(a.smem_bytes), stream, a.pdl != 0, a, tmk, tmv);
 }

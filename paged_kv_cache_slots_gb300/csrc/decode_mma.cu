@@ -23,6 +23,7 @@ namespace pkv {
 
 template <int DT, int D>
 struct MmaPolicy {
+    static constexpr int kMaxThreads = 32 * 16;
     static constexpr bool kTensor = true;
     static constexpr bool kScratch = false;
     static constexpr bool kPairs = false;
