@@ -93,6 +93,19 @@ def test_negative_zero_and_large_scale(head_dim, scale):
     _step(spec, [1, 40, 65, 3], scale=scale)
 
 
+@pytest.mark.parametrize("block_size", [32, 64, 128])
+@pytest.mark.parametrize("group", [1, 2, 8])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tensor_core_block_sizes_and_groups(block_size, group, dtype):
+    # The tcgen05 kernel's two loaders (per-lane copies below 64-token blocks,
+    # TMA boxes from 64 up) with every query-head group size; contexts cross
+    # block and 64-key tile boundaries and end mid-block.
+    ctx = (1, block_size + 3, 129, 2 * block_size + 64 + 7, 300)
+    spec = small_spec(f"prefill_tc_bs{block_size}_g{group}_{dtype}", num_q_heads=2 * group, num_kv_heads=2,
+                      head_dim=128, block_size=block_size, dtype=dtype, seed=31 + block_size + group, ctx=ctx)
+    _step(spec, new_token_counts(ctx, seed=group, max_chunk=200))
+
+
 def test_output_in_input_dtype():
     spec = small_spec("prefill_out_bf16", num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                       dtype="bf16", seed=7, ctx=(300, 17, 1, 64))
