@@ -10,8 +10,9 @@ import torch
 
 import oracle
 import paged_kv_cache_slots_gb300 as pkv
-from gpu_harness import bits, check_output
-from workloads import SPECS, make_placement, new_token_counts, pool_layer_values, small_spec, step_token_values
+from gpu_harness import bits, check_output, compact_blocks, take
+from workloads import (SPECS, fill_pool_layer, make_placement, new_token_counts, pool_layer_values, small_spec,
+                       step_token_values)
 
 pytestmark = pytest.mark.gpu
 
@@ -161,3 +162,54 @@ def test_bad_lengths_flagged_and_skipped():
     assert torch.isfinite(out[:4]).all()
     with pytest.raises(pkv.KVError):
         pkv.paged_prefill_attention(q.float(), k_pre.float(), v_pre.float(), tables, qs, ctx, 0.1)
+
+
+def test_chunked_prefill_b32_full_size_sampled():
+    # Layer 0 of the benchmarked step at full size (16,384 new tokens: 32 decodes
+    # at 4096 tokens of context and a 16,352-token chunk after 16,384 cached
+    # tokens), run by the library in one call.  The oracle recomputes sampled
+    # tokens, each as one query over its causal prefix, from the seeded
+    # pre-append pool and its own append of every new token of the sampled
+    # sequences.
+    spec = SPECS["chunked_prefill_b32"]
+    pl = make_placement(spec)
+    ctx = pl.context_lens
+    nq = np.asarray(spec.new_tokens, np.int32)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    T = int(qs[-1])
+    pool = pkv.KVPool(1, pl.num_blocks, spec.block_size, spec.num_kv_heads, spec.head_dim, spec.torch_dtype)
+    kc, vc = pool.layer(0)
+    fill_pool_layer(spec, 0, kc, vc)
+    q, kn, vn = step_token_values(spec, T, 0, "cuda")
+    long_s = int(np.argmax(nq))
+    seqs = [0, 17, long_s]
+    used, ctab = compact_blocks(pl.block_tables, seqs)
+    used_t = torch.from_numpy(used.astype(np.int64)).cuda()
+    k_pre, v_pre = take(kc, used_t).cpu(), take(vc, used_t).cpu()  # the oracle's pool: pre-append
+    tables = torch.from_numpy(pl.block_tables).cuda()
+    ctx_d = torch.from_numpy(ctx).cuda()
+    qs_d = torch.from_numpy(qs).cuda()
+    slots = pkv.slot_mapping_varlen(tables, qs_d, ctx_d, spec.block_size, pl.num_blocks, num_tokens=T)
+    pool.append(0, kn, vn, slots)
+    out = torch.full((T, spec.num_q_heads, spec.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+    pkv.paged_prefill_attention(q, kc, vc, tables, qs_d, ctx_d, spec.attn_scale, out=out, out_dtype=torch.float32)
+    assert pkv.device_status() == (0, 0)
+    # The oracle's append of every new token of the sampled sequences.
+    nq_s = nq[seqs]
+    qs_s = np.concatenate([[0], np.cumsum(nq_s)]).astype(np.int32)
+    rows = np.concatenate([np.arange(qs[s], qs[s + 1]) for s in seqs])
+    rows_t = torch.from_numpy(rows).cuda()
+    o_slots = oracle.slot_mapping_varlen(ctab, qs_s, ctx[seqs], spec.block_size)
+    k_post, v_post = oracle.append(k_pre, v_pre, kn[rows_t].cpu(), vn[rows_t].cpu(), o_slots)
+    assert torch.equal(bits(take(kc, used_t).cpu()), bits(k_post)), "K blocks after the append"
+    assert torch.equal(bits(take(vc, used_t).cpu()), bits(v_post)), "V blocks after the append"
+    # Sampled tokens: both decodes, and the chunk's first, last and three inner tokens.
+    picks = [(0, 0), (1, 0)] + [(2, i) for i in (0, 1, 4095, 8190, int(nq[long_s]) - 1)]
+    for k, i in picks:
+        s = seqs[k]
+        pos = int(ctx[s] - nq[s] + i)
+        t = int(qs[s] + i)
+        ref = oracle.paged_decode(q[t:t + 1].cpu(), k_post, v_post, ctab[k:k + 1],
+                                  np.array([pos + 1], np.int32), spec.attn_scale)
+        check_output(out[t:t + 1], ref, f"chunked_prefill_b32 sequence {s} token {i} (position {pos})")
+
