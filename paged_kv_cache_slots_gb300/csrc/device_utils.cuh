@@ -73,21 +73,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` waiting for the
+// phase (it resumes as soon as the phase completes), so a wait does not keep
+// issuing polls that the other warps of its scheduler could have used.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false and
-// raises the timeout flag) after kWaitLimitNs, or at once if *abort is set.
+// raises the timeout flag) after kWaitLimitNs, or at once if *abort is set
+// (checked at least every 10 us).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint32_t* status) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                raise_flag(status, kFlagTimeout);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            raise_flag(status, kFlagTimeout);
+            return false;
         }
     }
 }
