@@ -444,6 +444,25 @@ kv_status_t kv_allocator_slot(const kv_block_allocator_t* a, int64_t seq_id, int
 kv_status_t kv_allocator_free_queue(const kv_block_allocator_t* a, int32_t* out, int capacity,
                                     int* count_out);
 
+/* Sequence bookkeeping on the pool itself: the pool keeps one allocator of
+ * its blocks (the semantics above, no null block), created on first use.
+ * kv_seq_extend grows sequence seq_id by new_tokens tokens:
+ *   *ctx_len_inout  in: the sequence's current length (0 for a new one; it must
+ *                   match the pool's record), out: the new length;
+ *   table_row       host int32 [max_blocks]: the sequence's block table,
+ *                   padded with -1;
+ *   slot_out        host int32 [new_tokens] (may be NULL when new_tokens is 0):
+ *                   slot of each new token, block * block_size + offset
+ *                   ("vLLM Architecture and Installation", Example 3).
+ * A table that would not fit in max_blocks entries (KV_ERR_INVALID_ARG) or an
+ * extension that needs more blocks than are free (KV_ERR_OUT_OF_BLOCKS)
+ * changes nothing.  kv_seq_free returns the sequence's blocks to the back of
+ * the free queue (KV_ERR_NOT_FOUND for an unknown sequence).  Host-side and
+ * single-threaded per pool. */
+kv_status_t kv_seq_extend(kv_pool_t* pool, int seq_id, int new_tokens, int32_t* table_row, int max_blocks,
+                          int* ctx_len_inout, int32_t* slot_out);
+kv_status_t kv_seq_free(kv_pool_t* pool, int seq_id);
+
 /* ------------------------------------------ block pool with prefix caching */
 
 /* The block pool of "Reading Inference Engine Codebases", Examples 12 and 13

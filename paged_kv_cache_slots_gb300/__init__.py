@@ -89,6 +89,8 @@ def _declare(lib):
         "kv_allocator_create": (I, [I, I, I, ctypes.POINTER(P)]),
         "kv_allocator_destroy": (None, [P]),
         "kv_allocator_extend": (I, [P, I64, I]),
+        "kv_seq_extend": (I, [P, I, I, P, I, ctypes.POINTER(I), P]),
+        "kv_seq_free": (I, [P, I]),
         "kv_allocator_release": (I, [P, I64]),
         "kv_allocator_table": (I, [P, I64, ctypes.POINTER(ctypes.c_int32), I,
                                    ctypes.POINTER(I), ctypes.POINTER(I)]),
@@ -200,6 +202,22 @@ class KVPool:
     @property
     def num_layers(self):
         return self.cfg.num_layers
+
+    def seq_extend(self, seq_id: int, new_tokens: int, ctx_len: int, max_blocks: int):
+        """kv_seq_extend: grow sequence seq_id (currently ctx_len tokens) by
+        new_tokens on the pool's own allocator.  Returns (table row [max_blocks]
+        padded with -1, new length, slots of the new tokens), host int32 tensors."""
+        row = torch.full((max_blocks,), -1, dtype=torch.int32)
+        slots = torch.zeros(max(new_tokens, 1), dtype=torch.int32)
+        n = ctypes.c_int(ctx_len)
+        _check(self._lib.kv_seq_extend(self._handle, seq_id, new_tokens, ctypes.c_void_p(row.data_ptr()),
+                                       max_blocks, ctypes.byref(n), ctypes.c_void_p(slots.data_ptr())),
+               self._lib)
+        return row, n.value, slots[:new_tokens]
+
+    def seq_free(self, seq_id: int):
+        """kv_seq_free: return the sequence's blocks to the pool's free queue."""
+        _check(self._lib.kv_seq_free(self._handle, seq_id), self._lib)
 
     def layer(self, layer: int):
         """(K, V) torch views of one layer, addresses taken from kv_pool_layer."""

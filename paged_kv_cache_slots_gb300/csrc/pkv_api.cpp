@@ -209,6 +209,7 @@ struct kv_pool {
     char* base;
     bool owned;
     size_t layer_bytes;  // one of K or V for one layer
+    kv_block_allocator_t* alloc = nullptr;  // kv_seq_extend / kv_seq_free, created on first use
 };
 
 // ---------------------------------------------------------------- allocator
@@ -359,6 +360,7 @@ void kv_pool_destroy(kv_pool_t* p) {
         DeviceGuard g(p->cfg.device);
         cudaFree(p->base);
     }
+    kv_allocator_destroy(p->alloc);
     delete p;
 }
 
@@ -915,6 +917,41 @@ kv_status_t kv_allocator_slot(const kv_block_allocator_t* a, int64_t seq_id, int
         return fail(KV_ERR_INVALID_ARG, "position %d outside the sequence's blocks", position);
     *slot_out = t[position / a->block_size] * a->block_size + position % a->block_size;
     return KV_OK;
+}
+
+kv_status_t kv_seq_extend(kv_pool_t* p, int seq_id, int new_tokens, int32_t* table_row, int max_blocks,
+                          int* ctx_len_inout, int32_t* slot_out) {
+    if (!p || !table_row || !ctx_len_inout || max_blocks <= 0 || new_tokens < 0 || (new_tokens > 0 && !slot_out))
+        return fail(KV_ERR_INVALID_ARG, "kv_seq_extend arguments");
+    if (!p->alloc) {
+        if (kv_status_t st = kv_allocator_create(p->cfg.num_blocks, p->cfg.block_size, 0, &p->alloc)) return st;
+    }
+    kv_block_allocator* a = p->alloc;
+    auto it = a->seqs.find(seq_id);
+    const int64_t have = it == a->seqs.end() ? 0 : it->second.tokens;
+    if (*ctx_len_inout != have)
+        return fail(KV_ERR_INVALID_ARG, "sequence %d holds %lld tokens, the caller says %d", seq_id,
+                    static_cast<long long>(have), *ctx_len_inout);
+    const int64_t total = have + new_tokens;
+    const int64_t blocks = (total + a->block_size - 1) / a->block_size;
+    if (blocks > max_blocks)
+        return fail(KV_ERR_INVALID_ARG, "sequence %d would need %lld table entries, %d given", seq_id,
+                    static_cast<long long>(blocks), max_blocks);
+    if (kv_status_t st = kv_allocator_extend(a, seq_id, new_tokens)) return st;
+    const auto& t = a->seqs[seq_id].table;
+    for (int i = 0; i < max_blocks; ++i) table_row[i] = i < static_cast<int>(t.size()) ? t[i] : -1;
+    for (int i = 0; i < new_tokens; ++i) {
+        const int64_t pos = have + i;
+        slot_out[i] = t[pos / a->block_size] * a->block_size + static_cast<int32_t>(pos % a->block_size);
+    }
+    *ctx_len_inout = static_cast<int>(total);
+    return KV_OK;
+}
+
+kv_status_t kv_seq_free(kv_pool_t* p, int seq_id) {
+    if (!p) return fail(KV_ERR_INVALID_ARG, "null pool");
+    if (!p->alloc) return fail(KV_ERR_NOT_FOUND, "unknown sequence %d", seq_id);
+    return kv_allocator_release(p->alloc, seq_id);
 }
 
 kv_status_t kv_allocator_free_queue(const kv_block_allocator_t* a, int32_t* out, int capacity, int* count_out) {

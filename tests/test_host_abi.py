@@ -168,6 +168,45 @@ def test_pool_adopts_a_buffer_and_lays_out_layers(lib):
     assert lib.kv_pool_bytes(ctypes.byref(_cfg(dtype=7))) == 0
 
 
+def test_pool_sequence_bookkeeping(lib):
+    # kv_seq_extend / kv_seq_free on the pool's own allocator: blocks taken from
+    # the front of the free queue only when a token crosses a block boundary,
+    # slots = block * block_size + offset, tables padded with -1, released
+    # blocks to the back of the queue ("vLLM Architecture and Installation",
+    # Example 3).  The pool adopts a fake device address (never dereferenced).
+    cfg = _cfg()  # 10 blocks of 16 tokens
+    n = lib.kv_pool_bytes(ctypes.byref(cfg))
+    h = ctypes.c_void_p()
+    assert lib.kv_pool_create(ctypes.byref(cfg), ctypes.c_void_p(0x10000000), n, ctypes.byref(h)) == 0
+    row = (ctypes.c_int32 * 4)()
+    slots = (ctypes.c_int32 * 40)()
+    ln = ctypes.c_int(0)
+    assert lib.kv_seq_extend(h, 7, 20, row, 4, ctypes.byref(ln), slots) == 0
+    assert ln.value == 20 and list(row) == [0, 1, -1, -1]
+    assert list(slots[:20]) == list(range(20))
+    ln2 = ctypes.c_int(0)
+    assert lib.kv_seq_extend(h, 3, 5, row, 4, ctypes.byref(ln2), slots) == 0
+    assert list(row) == [2, -1, -1, -1] and list(slots[:5]) == [32, 33, 34, 35, 36]
+    # Growing 7 by 13 tokens: positions 20..32 -> block 1 offsets 4..15, then a new block 3.
+    assert lib.kv_seq_extend(h, 7, 13, row, 4, ctypes.byref(ln), slots) == 0
+    assert ln.value == 33 and list(row) == [0, 1, 3, -1]
+    assert list(slots[:13]) == [16 + o for o in range(4, 16)] + [48]
+    # A stale length, a table too short, more blocks than are free: errors that change nothing.
+    bad = ctypes.c_int(5)
+    assert lib.kv_seq_extend(h, 7, 1, row, 4, ctypes.byref(bad), slots) == 1
+    assert lib.kv_seq_extend(h, 7, 200, row, 4, ctypes.byref(ln), slots) == 1
+    big = (ctypes.c_int32 * 20)()
+    assert lib.kv_seq_extend(h, 8, 200, big, 20, ctypes.byref(ctypes.c_int(0)), (ctypes.c_int32 * 200)()) == 4
+    assert ln.value == 33
+    # Free 7: blocks 0, 1, 3 go to the back of the queue; a new sequence takes the front (4).
+    assert lib.kv_seq_free(h, 7) == 0
+    assert lib.kv_seq_free(h, 7) == 9
+    ln3 = ctypes.c_int(0)
+    assert lib.kv_seq_extend(h, 9, 1, row, 4, ctypes.byref(ln3), slots) == 0
+    assert list(row) == [4, -1, -1, -1] and slots[0] == 64
+    lib.kv_pool_destroy(h)
+
+
 def _attn(lib, **kw):
     A = 0x20000000
     args = dict(q=A, k=A, v=A, nb=64, tables=A, max_blocks=8, lens=A, B=4, hq=8, hkv=2, d=64, bs=16,
