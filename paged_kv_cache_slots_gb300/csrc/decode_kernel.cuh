@@ -245,7 +245,7 @@ static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* ful
 // l / G, head l % G in one load, the weights are shared by shuffles, and the
 // partial outputs of two parts (all G heads, D/32 dims per lane) are loaded
 // together before they are used.
-template <int G, int D>
+template <int G, int D, int kPre>
 __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, int hw, int pair,
                                             int ca, int cb, int64_t W) {
     constexpr int VD = D / 32;
@@ -275,6 +275,20 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, i
         const int n = __popc(__ballot_sync(0xffffffffu, my_c >= 0 && kg == 0));
         if (n == 0) break;
         c = __shfl_sync(0xffffffffu, my_c, (n - 1) * G) + 1;
+        // The partial outputs of the first kPre parts are loaded together with
+        // the (max, sum) pairs, so that a typical merge (a pair split over a
+        // handful of CTAs) waits for fewer rounds of loads.
+        float pre[kPre][G][VD];
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int ck = __shfl_sync(0xffffffffu, my_c, (k < n ? k : 0) * G);
+            const int64_t s0 = ((static_cast<int64_t>(ck) + pair) * Hc + hw) * G;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int i = 0; i < VD; ++i)
+                    pre[k][g][i] = k < n ? __ldcg(a.part_o + (s0 + g) * D + lane + 32 * i) : 0.f;
+        }
         float2 ml = make_float2(-INFINITY, 0.f);
         if (my_c >= 0) {
             const int64_t sl = ((static_cast<int64_t>(my_c) + pair) * Hc + hw) * G + kg;
@@ -298,8 +312,18 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, i
 #pragma unroll
         for (int g = 0; g < G; ++g)
             for (int k = 0; k < n; ++k) Lsum[g] += __shfl_sync(0xffffffffu, wl, k * G + g);
-        // Partial outputs, two parts per round of loads.
-        for (int k = 0; k < n; k += 2) {
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float w = __shfl_sync(0xffffffffu, w_lane, (k < n ? k : 0) * G + g);
+                if (k >= n) w = 0.f;
+#pragma unroll
+                for (int i = 0; i < VD; ++i) acc[g][i] += w * pre[k][g][i];
+            }
+        }
+        // The remaining partial outputs, two parts per round of loads.
+        for (int k = kPre; k < n; k += 2) {
             const int c0 = __shfl_sync(0xffffffffu, my_c, k * G);
             const int c1 = __shfl_sync(0xffffffffu, my_c, (k + 1 < n ? k + 1 : k) * G);
             const int64_t s0 = ((static_cast<int64_t>(c0) + pair) * Hc + hw) * G;
@@ -332,19 +356,37 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, i
     }
 }
 
-template <int G, int D>
+// Count one arrival on a merge counter (gpu scope, acquire + release): the
+// writes ordered before it (the warp's partial, through the warp barrier
+// before it) are visible to whoever counts later, and the partials of every
+// warp that counted before are visible after it.
+__device__ __forceinline__ int counter_arrive(int32_t* counter) {
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
+    return prev;
+}
+
+// Parts whose outputs the merge loads together with the (max, sum) pairs:
+// up to 48 values a lane in a kernel built for at most 384 threads (168
+// registers a thread), 16 in one built for 512 (128 registers); 1 to 4.
+__host__ __device__ constexpr int merge_prefetch(int G, int D, int max_threads) {
+    const int per_part = G * (D / 32);
+    const int k = (max_threads <= 32 * 12 ? 48 : 16) / per_part;
+    return k < 1 ? 1 : (k > 4 ? 4 : k);
+}
+
+template <int G, int D, int kPre>
 __device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, int pair, int nparts,
                               int ca, int cb, int64_t W) {
     const int lane = threadIdx.x & 31;
     int32_t* counter = a.counters + static_cast<int64_t>(s) * a.num_kv_heads + h;
-    __threadfence();
-    __syncwarp();
+    __syncwarp();  // the warp's partial stores come before lane 0's release
     int prev = 0;
-    if (lane == 0) prev = atomicAdd(counter, 1);
+    if (lane == 0) prev = counter_arrive(counter);
     prev = __shfl_sync(0xffffffffu, prev, 0);
     if (prev != nparts - 1) return;
-    __threadfence();
-    merge_parts<G, D>(a, s, h, hw, pair, ca, cb, W);
+    __syncwarp();  // and every lane's loads after lane 0's acquire
+    merge_parts<G, D, kPre>(a, s, h, hw, pair, ca, cb, W);
     __syncwarp();
     if (lane == 0) *counter = 0;
 }
@@ -604,11 +646,20 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
                 nparts = 0;
                 for (int c = ca; c <= cb; ++c) nparts += !cta_is_empty(c, W, P);
             }
+            constexpr int T = Policy::kMaxThreads, DD = Policy::kD;
             switch (G) {
-                case 1: merge_if_last<1, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
-                case 2: merge_if_last<2, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
-                case 4: merge_if_last<4, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
-                default: merge_if_last<8, Policy::kD>(a, s, h, hw, pair, nparts, ca, cb, W); break;
+                case 1:
+                    merge_if_last<1, DD, merge_prefetch(1, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    break;
+                case 2:
+                    merge_if_last<2, DD, merge_prefetch(2, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    break;
+                case 4:
+                    merge_if_last<4, DD, merge_prefetch(4, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    break;
+                default:
+                    merge_if_last<8, DD, merge_prefetch(8, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    break;
             }
         }
         seg = seg_end;

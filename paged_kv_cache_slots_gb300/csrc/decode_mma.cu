@@ -21,9 +21,9 @@
 
 namespace pkv {
 
-template <int DT, int D>
+template <int DT, int D, int kMaxT = 32 * 16>
 struct MmaPolicy {
-    static constexpr int kMaxThreads = 32 * 16;
+    static constexpr int kMaxThreads = kMaxT;
     static constexpr bool kTensor = true;
     static constexpr bool kScratch = false;
     static constexpr bool kPairs = false;
@@ -274,9 +274,13 @@ struct MmaPolicy {
     }
 };
 
+// Launches of up to 12 warps (the default is 9) use the instantiation built
+// for 384 threads, whose register budget (168 a thread) holds the consumer
+// state and the merge of split pairs without spilling.
 template <int DT, int D>
 static cudaError_t launch_mma_t(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                 cudaStream_t stream) {
+    if (32 * (1 + a.consumer_warps) <= 32 * 12) return launch_partial<MmaPolicy<DT, D, 32 * 12>>(a, tmk, tmv, stream);
     return launch_partial<MmaPolicy<DT, D>>(a, tmk, tmv, stream);
 }
 
