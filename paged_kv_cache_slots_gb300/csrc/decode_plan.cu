@@ -45,8 +45,15 @@ bool decode_plan(int kernel, int dtype, int head_dim, int block_size, int group,
 // several CTAs (log-sum-exp in base 2), zero the rows of an empty sequence,
 // skip pairs the partial kernel finished itself.  CTAs between the first and
 // last owner whose item range is empty (more CTAs than items) wrote nothing
-// and are skipped.
+// and are skipped.  Parts are taken 32 at a time: warp 0 reads their (max,
+// sum) pairs, one part a lane, and folds them into each head's running max
+// and sum, leaving the parts' weights in shared memory; then every thread
+// rescales its outputs and adds the parts' outputs, several loads in flight.
 __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeArgs a) {
+    constexpr int kChunk = 32, kMaxG = 8, kPer = kMaxG * 128 / 128;  // outputs a thread, G*D <= 1024
+    __shared__ float wgt[kChunk][kMaxG];  // exp2(m - M) of (part, head) in the current chunk
+    __shared__ float rescale[kMaxG];      // exp2(M_old - M) of each head for this chunk
+    __shared__ float run_m[kMaxG], run_l[kMaxG];
     pdl_allow_next();
     pdl_wait();
     const int sh = blockIdx.x;
@@ -58,8 +65,9 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeAr
     const int hc = h / Hc, hw = h - hc * Hc;
     const int nb = (a.cum[s + 1] - a.cum[s]) / chunks;
     const int64_t out0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
+    const int tid = threadIdx.x;
     if (nb == 0) {
-        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) store_out(a.out, out0 + idx, 0.f, a.out_dtype);
+        for (int idx = tid; idx < G * D; idx += blockDim.x) store_out(a.out, out0 + idx, 0.f, a.out_dtype);
         return;
     }
     const int64_t W = a.cum[a.num_seqs];
@@ -69,22 +77,70 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeAr
     const int cb = cta_of_item(pa + nb - 1, W, a.num_ctas);
     if (ca == cb) return;
     const int pair = s * chunks + hc;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int g = idx / D, d = idx - g * D;
-        float M = -INFINITY;
-        for (int c = ca; c <= cb; ++c) {
-            if (cta_is_empty(c, W, P)) continue;
-            M = fmaxf(M, a.part_ml[(((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g) * 2]);
+    if (tid < kMaxG) {
+        run_m[tid] = -INFINITY;
+        run_l[tid] = 0.f;
+    }
+    float acc[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+    for (int c0 = ca; c0 <= cb; c0 += kChunk) {
+        __syncthreads();  // the previous chunk's weights are used up
+        if (tid < 32) {
+            const int c = c0 + tid;
+            const bool valid = c <= cb && !cta_is_empty(c, W, P);
+            const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G;
+            for (int g = 0; g < G; ++g) {
+                float m = -INFINITY, l = 0.f;
+                if (valid) {
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sl + g) * 2));
+                    m = ml.x;
+                    l = ml.y;
+                }
+                float mx = m;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float m_old = run_m[g];
+                const float m_new = fmaxf(m_old, mx);
+                const float w = valid ? fast_exp2(m - m_new) : 0.f;
+                wgt[tid][g] = w;
+                float ls = w * l;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+                __syncwarp();
+                if (tid == 0) {
+                    const float al = m_old == -INFINITY ? 0.f : fast_exp2(m_old - m_new);
+                    rescale[g] = al;
+                    run_l[g] = run_l[g] * al + ls;
+                    run_m[g] = m_new;
+                }
+                __syncwarp();
+            }
         }
-        float Lsum = 0.f, O = 0.f;
-        for (int c = ca; c <= cb; ++c) {
-            if (cta_is_empty(c, W, P)) continue;
-            const int64_t sl = ((static_cast<int64_t>(c) + pair) * Hc + hw) * G + g;
-            const float wgt = fast_exp2(a.part_ml[sl * 2] - M);
-            Lsum += wgt * a.part_ml[sl * 2 + 1];
-            O += wgt * a.part_o[sl * D + d];
+        __syncthreads();
+        const int nc = min(kChunk, cb - c0 + 1);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = tid + 128 * k;
+            if (idx < G * D) acc[k] *= rescale[idx / D];
         }
-        store_out(a.out, out0 + idx, O / Lsum, a.out_dtype);
+#pragma unroll 4
+        for (int j = 0; j < nc; ++j) {
+            const int64_t base = ((static_cast<int64_t>(c0 + j) + pair) * Hc + hw) * G * D;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int idx = tid + 128 * k;
+                if (idx >= G * D) continue;
+                const float w = wgt[j][idx / D];
+                if (w != 0.f) acc[k] += w * __ldcg(a.part_o + base + idx);  // empty parts hold no data
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int idx = tid + 128 * k;
+        if (idx < G * D) store_out(a.out, out0 + idx, acc[k] / run_l[idx / D], a.out_dtype);
     }
 }
 
