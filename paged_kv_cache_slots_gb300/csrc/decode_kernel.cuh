@@ -356,6 +356,95 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, i
     }
 }
 
+// The merge of a pair split over n <= 32/G parts ca .. ca+n-1, none empty.
+// Lane l loads (max, sum) of part l / G, head l % G; xor shuffles over lanes
+// holding the same head give each head's max M and sum L in one round.  The
+// outputs are then summed part by part in slot order (one fma per part), so
+// the result does not depend on where they are read from:
+// - scratch: this warp's slice of the CTA's ring, free at the end of the
+//   CTA's item range; every part's outputs are copied there in one round of
+//   16-byte copies issued together with the (max, sum) loads;
+// - otherwise from L2, kPre parts per round of loads.
+template <int G, int D, int kPre>
+__device__ __forceinline__ void merge_parts_small(const DecodeArgs& a, int s, int h, int hw, int pair,
+                                                  int ca, int n, float* scratch) {
+    constexpr int VD = D / 32;
+    constexpr int kPart = G * D;  // floats of one part's outputs
+    const int lane = threadIdx.x & 31;
+    const int Hc = a.heads_per_stage;
+    auto part_out = [&](int k) {
+        return a.part_o + ((static_cast<int64_t>(ca + k) + pair) * Hc + hw) * kPart;
+    };
+    if (scratch) {
+        const uint32_t dst0 = smem_addr(scratch);
+        for (int e = lane; e < n * (kPart / 4); e += 32) {
+            const int k = e / (kPart / 4);
+            cp_async_16(dst0 + 16u * static_cast<uint32_t>(e), part_out(k) + 4 * (e - k * (kPart / 4)));
+        }
+    }
+    const int kp = lane / G, kg = lane % G;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (kp < n)
+        ml = __ldcg(reinterpret_cast<const float2*>(
+            a.part_ml + (((static_cast<int64_t>(ca + kp) + pair) * Hc + hw) * G + kg) * 2));
+    float M = ml.x;
+#pragma unroll
+    for (int o = G; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = kp < n ? fast_exp2(ml.x - M) : 0.f;
+    float L = w * ml.y;
+#pragma unroll
+    for (int o = G; o < 32; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    float acc[G][VD];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < VD; ++i) acc[g][i] = 0.f;
+    if (scratch) {
+        cp_async_wait_all();
+        __syncwarp();
+        for (int k = 0; k < n; ++k) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float wk = __shfl_sync(0xffffffffu, w, k * G + g);
+#pragma unroll
+                for (int i = 0; i < VD; ++i)
+                    acc[g][i] = fmaf(wk, scratch[k * kPart + g * D + lane + 32 * i], acc[g][i]);
+            }
+        }
+    } else {
+        for (int k0 = 0; k0 < n; k0 += kPre) {
+            float v[kPre][G][VD];
+#pragma unroll
+            for (int j = 0; j < kPre; ++j) {
+                const float* src = part_out(k0 + j < n ? k0 + j : 0);
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int i = 0; i < VD; ++i)
+                        v[j][g][i] = k0 + j < n ? __ldcg(src + g * D + lane + 32 * i) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < kPre; ++j) {
+                if (k0 + j >= n) break;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float wk = __shfl_sync(0xffffffffu, w, (k0 + j) * G + g);
+#pragma unroll
+                    for (int i = 0; i < VD; ++i) acc[g][i] = fmaf(wk, v[j][g][i], acc[g][i]);
+                }
+            }
+        }
+    }
+    const int64_t o0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float inv = 1.f / __shfl_sync(0xffffffffu, L, g);  // lane g: part 0, head g
+#pragma unroll
+        for (int i = 0; i < VD; ++i)
+            store_out(a.out, o0 + g * D + lane + 32 * i, acc[g][i] * inv, a.out_dtype);
+    }
+}
+
 // Count one arrival on a merge counter (gpu scope, acquire + release): the
 // writes ordered before it (the warp's partial, through the warp barrier
 // before it) are visible to whoever counts later, and the partials of every
@@ -375,9 +464,11 @@ __host__ __device__ constexpr int merge_prefetch(int G, int D, int max_threads) 
     return k < 1 ? 1 : (k > 4 ? 4 : k);
 }
 
+// scratch: this warp's slice of the free ring (scratch_floats floats), or
+// null when the ring is still in use.
 template <int G, int D, int kPre>
 __device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, int pair, int nparts,
-                              int ca, int cb, int64_t W) {
+                              int ca, int cb, int64_t W, float* scratch, int scratch_floats) {
     const int lane = threadIdx.x & 31;
     int32_t* counter = a.counters + static_cast<int64_t>(s) * a.num_kv_heads + h;
     __syncwarp();  // the warp's partial stores come before lane 0's release
@@ -386,7 +477,14 @@ __device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, int pai
     prev = __shfl_sync(0xffffffffu, prev, 0);
     if (prev != nparts - 1) return;
     __syncwarp();  // and every lane's loads after lane 0's acquire
-    merge_parts<G, D, kPre>(a, s, h, hw, pair, ca, cb, W);
+    // Which warp merges depends on timing, so the choice of path depends on
+    // the pair only; the ring (when free) changes where the loads come from,
+    // not the arithmetic.
+    if (W >= a.num_ctas && nparts * G <= 32)
+        merge_parts_small<G, D, kPre>(a, s, h, hw, pair, ca, nparts,
+                                      nparts * G * D <= scratch_floats ? scratch : nullptr);
+    else
+        merge_parts<G, D, kPre>(a, s, h, hw, pair, ca, cb, W);
     __syncwarp();
     if (lane == 0) *counter = 0;
 }
@@ -638,6 +736,17 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
             }
             named_barrier_sync(1, NC * 32);
         }
+        // A split pair at the end of the range: once every consumer warp is
+        // past its last stage, the ring's shared memory is free (the producer
+        // issued nothing after the range's last item) and the merge may stage
+        // the parts there, one slice a warp.
+        float* staging = nullptr;
+        int staging_floats = 0;
+        if (R == 1 && a.fused_reduce && seg_end == end && !whole) {
+            named_barrier_sync(1, NC * 32);
+            staging_floats = (a.stages * 2 * half_bytes / NC / 4) & ~3;
+            staging = reinterpret_cast<float*>(ring) + w * staging_floats;
+        }
         if (partial && a.fused_reduce) {
             const int ca = cta_of_item(pair_a, W, P);
             const int cb = cta_of_item(pair_b - 1, W, P);
@@ -649,16 +758,20 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
             constexpr int T = Policy::kMaxThreads, DD = Policy::kD;
             switch (G) {
                 case 1:
-                    merge_if_last<1, DD, merge_prefetch(1, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    merge_if_last<1, DD, merge_prefetch(1, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W,
+                                                                  staging, staging_floats);
                     break;
                 case 2:
-                    merge_if_last<2, DD, merge_prefetch(2, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    merge_if_last<2, DD, merge_prefetch(2, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W,
+                                                                  staging, staging_floats);
                     break;
                 case 4:
-                    merge_if_last<4, DD, merge_prefetch(4, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    merge_if_last<4, DD, merge_prefetch(4, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W,
+                                                                  staging, staging_floats);
                     break;
                 default:
-                    merge_if_last<8, DD, merge_prefetch(8, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W);
+                    merge_if_last<8, DD, merge_prefetch(8, DD, T)>(a, s, h, hw, pair, nparts, ca, cb, W,
+                                                                  staging, staging_floats);
                     break;
             }
         }

@@ -165,6 +165,15 @@ __device__ __forceinline__ void pdl_allow_next() {
 // L2-coherent load (bypasses L1): for data other CTAs wrote in this launch.
 __device__ __forceinline__ float load_cg(const float* p) { return __ldcg(p); }
 
+// 16 bytes global -> shared through L2 only (cp.async.cg), completed by
+// cp_async_wait_all() in the same thread.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // ----------------------------------------------------------- named barrier
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -180,6 +180,33 @@ def test_workspace_is_reusable_across_calls():
     assert int(ws[:3 * 2 * 4].view(torch.int32).abs().sum().item()) == 0
 
 
+@pytest.mark.parametrize("num_ctas", [40, 152])
+def test_split_merge_is_bitwise_reproducible(num_ctas):
+    """Which warp merges a split sequence depends on timing, and a warp at the
+    end of its CTA's range reads the parts through shared memory while any
+    other reads them from L2; the output bits must not depend on either.
+    40 CTAs: about six parts per sequence (the merge that loads every part in
+    one round); 152 CTAs: about twenty (the merge in rounds)."""
+    spec = SPECS["llama8b_layer_b8"]
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    _, _, _, ref = case.oracle()
+    d = case.device()
+    slots = pkv.slot_mapping(d["tables"], d["ctx"], spec.block_size, pl.num_blocks)
+    d["pool"].append(0, d["kn"], d["vn"], slots, seq_ids=d["seq_ids"])
+    ws = pkv.make_workspace(8, 32, 8, 128, num_ctas=num_ctas)
+    outs = []
+    for _ in range(6):
+        out = torch.full((8, 32, 128), float("nan"), device="cuda")
+        pkv.paged_decode_attention(d["q"], d["kc"], d["vc"], d["tables"], d["ctx"], spec.attn_scale,
+                                   out=out, out_dtype=torch.float32, workspace=ws, num_ctas=num_ctas)
+        outs.append(out)
+    check_output(outs[0], ref, f"{num_ctas} CTAs")
+    for o in outs[1:]:
+        assert torch.equal(bits(o), bits(outs[0]))
+    assert pkv.device_status() == (0, 0)
+
+
 @pytest.mark.parametrize("kernel", ["mma", "ffma"])
 def test_block_relabelling_is_bitwise_invariant(kernel):
     spec = small_spec("relabel", num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
