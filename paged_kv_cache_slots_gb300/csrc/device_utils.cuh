@@ -124,6 +124,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Bring `bytes` of global memory into L2 (bytes % 16 == 0, 16-byte aligned
+// address); no completion, a hint only.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled tensor copy (box given by the tensor map) completed on `bar`.
 __device__ __forceinline__ void tensor_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                                uint64_t* bar, uint64_t policy) {
