@@ -55,6 +55,9 @@ struct MmaFp8Policy {
     static constexpr int KS = D / 16;  // 16-dim chunks: k-slices of QK, m-slices of PV
     static constexpr int K8 = D / 32;  // 32-dim k-slices of the E4M3 QK
     static constexpr int kD = D;
+    // V enters the P.V product as its E4M3 value times 2^-8 (see
+    // e4m3x2_to_half2_shifted); the outputs are scaled back by 2^8, exactly.
+    static constexpr float kVUnscale = 256.f;
     using T = typename Elem<QT>::T;
 
     struct State {
@@ -282,13 +285,11 @@ struct MmaFp8Policy {
                 // r[2hf] holds tokens 0-7 and r[2hf+1] tokens 8-15 of chunk 2mp + hf.
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const uint32_t lo = __byte_perm(r[2 * hf], 0u, 0x3120u);
-                    const uint32_t hi = __byte_perm(r[2 * hf + 1], 0u, 0x3120u);
                     uint32_t af[4];
-                    af[0] = e4m3x2_to_half2(static_cast<uint16_t>(lo));        // dim 2g,   tokens 2c, 2c+1
-                    af[1] = e4m3x2_to_half2(static_cast<uint16_t>(lo >> 16));  // dim 2g+1, tokens 2c, 2c+1
-                    af[2] = e4m3x2_to_half2(static_cast<uint16_t>(hi));        // dim 2g,   tokens 8+2c, 9+2c
-                    af[3] = e4m3x2_to_half2(static_cast<uint16_t>(hi >> 16));  // dim 2g+1, tokens 8+2c, 9+2c
+                    af[0] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4240u));      // dim 2g,   tokens 2c, 2c+1
+                    af[1] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4341u));      // dim 2g+1, tokens 2c, 2c+1
+                    af[2] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4240u));  // dim 2g,   tokens 8+2c, 9+2c
+                    af[3] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4341u));  // dim 2g+1, tokens 8+2c, 9+2c
                     mma16816<kF16>(st.o[2 * mp + hf], af, bh[n][0], bh[n][1]);
                     if (!packed) mma16816<kF16>(st.o[2 * mp + hf], af, bl[n][0], bl[n][1]);
                 }
@@ -403,12 +404,12 @@ struct MmaFp8Policy {
 
     __device__ __forceinline__ void write_state(const State& st, const DecodeArgs& a, float* dst,
                                                 int stride, int G) const {
-        emit(st, a.v_scale, dst, stride, dst + D, stride, G);
+        emit(st, a.v_scale * kVUnscale, dst, stride, dst + D, stride, G);
     }
 
     __device__ __forceinline__ void write_partial(const State& st, const DecodeArgs& a, float* o,
                                                   float* ml, int G) const {
-        emit(st, a.v_scale, o, D, ml, 2, G);
+        emit(st, a.v_scale * kVUnscale, o, D, ml, 2, G);
     }
 
     // out[s][h*G + head][d] = v_scale * O / l in the output type.
@@ -418,7 +419,7 @@ struct MmaFp8Policy {
         const int g = lane >> 2, c = lane & 3;
         float l0, l1;
         row_sums(st, l0, l1);
-        const float i0 = a.v_scale / l0, i1 = a.v_scale / l1;
+        const float i0 = a.v_scale * kVUnscale / l0, i1 = a.v_scale * kVUnscale / l1;
         const int h0 = 2 * c, h1 = 2 * c + 1;
         const int64_t base = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
 #pragma unroll

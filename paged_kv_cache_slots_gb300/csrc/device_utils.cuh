@@ -255,6 +255,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t v) {
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// Two E4M3 codes in bytes 0 and 2 of y (bytes 1 and 3 zero) -> f16x2 of
+// their values times 2^-8, exactly, in integer operations: an E4M3 code
+// s.eeee.mmm read as the f16 bit pattern s.0eeee.mmm0000000 has exponent
+// field eeee, i.e. the same value scaled by 2^(7 - 15), subnormals included.
+// The magnitude moves up 7 bits and the sign 8: (y + (y & 0x80)) << 7 does
+// both in each 16-bit half without carries between the halves.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2_shifted(uint32_t y) {
+    return (y + (y & 0x00800080u)) << 7;
+}
+
 // Store an fp32 value as out_dtype (round to nearest even).
 __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int out_dtype) {
     if (out_dtype == kF32)
