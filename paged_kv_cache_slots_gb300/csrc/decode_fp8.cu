@@ -58,6 +58,8 @@ struct MmaFp8Policy {
     // V enters the P.V product as its E4M3 value times 2^-8 (see
     // e4m3x2_to_half2_shifted); the outputs are scaled back by 2^8, exactly.
     static constexpr float kVUnscale = 256.f;
+    // Likewise K in the f16 form of Q.K^T (not kQ8, where the MMA takes the codes).
+    static constexpr float kKUnscale = 256.f;
     using T = typename Elem<QT>::T;
 
     struct State {
@@ -200,10 +202,11 @@ struct MmaFp8Policy {
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {  // chunk 2kp + hf: rows g / g+8 in r[2hf] / r[2hf+1]
                         uint32_t af[4];
-                        af[0] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf]));
-                        af[1] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1]));
-                        af[2] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf] >> 16));
-                        af[3] = e4m3x2_to_half2(static_cast<uint16_t>(r[2 * hf + 1] >> 16));
+                        // K codes as f16 values times 2^-8 (kKUnscale restores the scores)
+                        af[0] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4140u));
+                        af[1] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4140u));
+                        af[2] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4342u));
+                        af[3] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4342u));
                         mma16816<kF16>(part[hf], af, st.qb[2 * kp + hf][0], st.qb[2 * kp + hf][1]);
                     }
                 }
@@ -215,8 +218,8 @@ struct MmaFp8Policy {
                 for (int r = 0; r < 4; ++r) acc[n][r] += __shfl_xor_sync(0xffffffffu, acc[n][r], 2);
             }
         }
-        const float sl0 = kQ8 ? st.sc[0] : a.scale_log2;
-        const float sl1 = kQ8 ? st.sc[1] : a.scale_log2;
+        const float sl0 = kQ8 ? st.sc[0] : a.scale_log2 * kKUnscale;
+        const float sl1 = kQ8 ? st.sc[1] : a.scale_log2 * kKUnscale;
         // ---- online softmax over all NS slices (heads 2c, 2c+1; tokens g, g+8 of each)
         float x[NS][4];
         float mx0 = -INFINITY, mx1 = -INFINITY;
