@@ -42,6 +42,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_mma.cu", "decode_ffma.cu", "decode_fp8.cu", "mma_frag.cuh",
                   "device_utils.cuh", "decode_plan.cu")
+L2_BYTES = 129 * 10**6  # GB300 L2
 PREFILL_SOURCES = ("prefill_tc.cu", "prefill.cu", "tc_utils.cuh", "decode_kernel.cuh", "mma_frag.cuh",
                    "device_utils.cuh")
 
@@ -297,20 +298,36 @@ def bench_ours(args, world, rank, local):
             graph.replay()
     torch.cuda.synchronize()
 
-    # Timed region: K replays.
+    # Timed region: K replays.  A step that reads less than 4x the L2 would
+    # find part of its K/V still in L2 from the step before: there every
+    # replay is timed on its own, after a write of twice the L2 outside the
+    # events.
+    flush = kv_bytes_step < 4 * L2_BYTES
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    if flush:
+        scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
     with ClockSampler(torch.cuda.current_device()) as clocks:
         barrier(world)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            e1.record(stream)
+            if flush:
+                for a0, a1 in pairs:
+                    scrub.fill_(1)
+                    a0.record(stream)
+                    graph.replay()
+                    a1.record(stream)
+            else:
+                e0.record(stream)
+                for _ in range(args.steps):
+                    graph.replay()
+                e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    local_ms = sum(a0.elapsed_time(a1) for a0, a1 in pairs) if flush else e0.elapsed_time(e1)
+    ms_total = max_over_ranks(local_ms, world, dev)
     ms_step = ms_total / args.steps
     clock = clocks.summary()
     st, flags = pkv.device_status(dev)
@@ -395,7 +412,9 @@ def bench_ours(args, world, rank, local):
                    "num_layers": spec.num_layers, "num_seqs": B, "context_tokens": int(pl.context_lens.sum()),
                    "kv_bytes_per_step": kv_bytes_step, "kernel": step.kernel,
                    "timing": "CUDA-graph replay of the whole step, CUDA events on the replay stream",
-                   "l2": "no flush: each step reads %.1f GB of K/V (> 129 MB L2)" % (kv_bytes_step / 1e9),
+                   "l2": ("L2 flushed (a %d MB write) before each timed replay: the step reads %.2f GB of K/V"
+                          % (2 * L2_BYTES // 10**6, kv_bytes_step / 1e9)) if flush else
+                         "no flush: each step reads %.1f GB of K/V (> 129 MB L2)" % (kv_bytes_step / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "decode_tokens_per_s": round(sum_over_ranks(B, world, dev) / (ms_step * 1e-3), 1),
         "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
