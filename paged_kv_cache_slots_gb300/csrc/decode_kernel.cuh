@@ -372,59 +372,97 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, i
     }
 }
 
-// The merge of a pair split over n <= 32/G parts ca .. ca+n-1, none empty.
-// Lane l loads (max, sum) of part l / G, head l % G; xor shuffles over lanes
-// holding the same head give each head's max M and sum L in one round.  The
-// outputs are then summed part by part in slot order (one fma per part), so
-// the result does not depend on where they are read from:
-// - scratch: this warp's slice of the CTA's ring, free at the end of the
-//   CTA's item range; every part's outputs are copied there in one round of
-//   16-byte copies issued together with the (max, sum) loads;
+// The merge of a pair split over n <= kSlots * 32/G parts ca .. ca+n-1, none
+// empty.  Lane l loads (max, sum) of parts l / G + j * 32/G, head l % G
+// (j < kSlots);
+// xor shuffles over lanes holding the same head give each head's max M and
+// sum L in one round.  The outputs are then summed part by part in slot
+// order (one fma per part), so the result does not depend on where they are
+// read from:
+// - scratch: this warp's slice of the CTA's ring (scratch_parts parts), free
+//   at the end of the CTA's item range; the parts' outputs are copied there
+//   in chunks of 16-byte copies, the first issued together with the (max,
+//   sum) loads: one round of loads per chunk;
 // - otherwise from L2, kPre parts per round of loads.
-template <int G, int D, int kPre>
+template <int G, int D, int kPre, int kSlots>
 __device__ __forceinline__ void merge_parts_small(const DecodeArgs& a, int s, int h, int hw, int pair,
-                                                  int ca, int n, float* scratch) {
+                                                  int ca, int n, float* scratch, int scratch_parts) {
     constexpr int VD = D / 32;
     constexpr int kPart = G * D;  // floats of one part's outputs
+    constexpr int kLaneParts = 32 / G;  // parts per round of (max, sum) loads
     const int lane = threadIdx.x & 31;
     const int Hc = a.heads_per_stage;
     auto part_out = [&](int k) {
         return a.part_o + ((static_cast<int64_t>(ca + k) + pair) * Hc + hw) * kPart;
     };
-    if (scratch) {
+    auto stage_parts = [&](int k0, int k1) {  // parts [k0, k1) to scratch
         const uint32_t dst0 = smem_addr(scratch);
-        for (int e = lane; e < n * (kPart / 4); e += 32) {
+        for (int e = lane; e < (k1 - k0) * (kPart / 4); e += 32) {
             const int k = e / (kPart / 4);
-            cp_async_16(dst0 + 16u * static_cast<uint32_t>(e), part_out(k) + 4 * (e - k * (kPart / 4)));
+            cp_async_16(dst0 + 16u * static_cast<uint32_t>(e), part_out(k0 + k) + 4 * (e - k * (kPart / 4)));
+        }
+    };
+    const int chunk = scratch ? scratch_parts : 0;
+    if (chunk) stage_parts(0, min(n, chunk));
+    const int kp = lane / G, kg = lane % G;
+    float m[kSlots], l[kSlots];
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+        m[j] = -INFINITY;
+        l[j] = 0.f;
+        const int k = kp + j * kLaneParts;
+        if (k < n) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                a.part_ml + (((static_cast<int64_t>(ca + k) + pair) * Hc + hw) * G + kg) * 2));
+            m[j] = ml.x;
+            l[j] = ml.y;
         }
     }
-    const int kp = lane / G, kg = lane % G;
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (kp < n)
-        ml = __ldcg(reinterpret_cast<const float2*>(
-            a.part_ml + (((static_cast<int64_t>(ca + kp) + pair) * Hc + hw) * G + kg) * 2));
-    float M = ml.x;
+    float M = m[0];
+#pragma unroll
+    for (int j = 1; j < kSlots; ++j) M = fmaxf(M, m[j]);
 #pragma unroll
     for (int o = G; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float w = kp < n ? fast_exp2(ml.x - M) : 0.f;
-    float L = w * ml.y;
+    float w[kSlots];
+    float L = 0.f;
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+        w[j] = kp + j * kLaneParts < n ? fast_exp2(m[j] - M) : 0.f;
+        L += w[j] * l[j];
+    }
 #pragma unroll
     for (int o = G; o < 32; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    // Weight of part k, head g (k < n): held by lane (k % kLaneParts) * G + g, slot k / kLaneParts.
+    auto weight = [&](int k, int g) {
+        const int j = k / kLaneParts;  // the same on every lane
+        float wj = w[0];
+#pragma unroll
+        for (int t = 1; t < kSlots; ++t)
+            if (j == t) wj = w[t];
+        return __shfl_sync(0xffffffffu, wj, (k % kLaneParts) * G + g);
+    };
     float acc[G][VD];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int i = 0; i < VD; ++i) acc[g][i] = 0.f;
-    if (scratch) {
-        cp_async_wait_all();
-        __syncwarp();
-        for (int k = 0; k < n; ++k) {
+    if (chunk) {
+        for (int k0 = 0; k0 < n; k0 += chunk) {
+            const int k1 = min(n, k0 + chunk);
+            if (k0 > 0) {
+                __syncwarp();  // the previous chunk is read
+                stage_parts(k0, k1);
+            }
+            cp_async_wait_all();
+            __syncwarp();
+            for (int k = k0; k < k1; ++k) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float wk = __shfl_sync(0xffffffffu, w, k * G + g);
+                for (int g = 0; g < G; ++g) {
+                    const float wk = weight(k, g);
 #pragma unroll
-                for (int i = 0; i < VD; ++i)
-                    acc[g][i] = fmaf(wk, scratch[k * kPart + g * D + lane + 32 * i], acc[g][i]);
+                    for (int i = 0; i < VD; ++i)
+                        acc[g][i] = fmaf(wk, scratch[(k - k0) * kPart + g * D + lane + 32 * i], acc[g][i]);
+                }
             }
         }
     } else {
@@ -444,7 +482,7 @@ __device__ __forceinline__ void merge_parts_small(const DecodeArgs& a, int s, in
                 if (k0 + j >= n) break;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float wk = __shfl_sync(0xffffffffu, w, (k0 + j) * G + g);
+                    const float wk = weight(k0 + j, g);
 #pragma unroll
                     for (int i = 0; i < VD; ++i) acc[g][i] = fmaf(wk, v[j][g][i], acc[g][i]);
                 }
@@ -454,7 +492,7 @@ __device__ __forceinline__ void merge_parts_small(const DecodeArgs& a, int s, in
     const int64_t o0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const float inv = 1.f / __shfl_sync(0xffffffffu, L, g);  // lane g: part 0, head g
+        const float inv = 1.f / __shfl_sync(0xffffffffu, L, g);  // lane g holds head g's sum
 #pragma unroll
         for (int i = 0; i < VD; ++i)
             store_out(a.out, o0 + g * D + lane + 32 * i, acc[g][i] * inv, a.out_dtype);
@@ -472,11 +510,11 @@ __device__ __forceinline__ int counter_arrive(int32_t* counter) {
 }
 
 // Parts whose outputs the merge loads together with the (max, sum) pairs:
-// up to 48 values a lane in a kernel built for at most 384 threads (168
+// up to 32 values a lane in a kernel built for at most 384 threads (168
 // registers a thread), 16 in one built for 512 (128 registers); 1 to 4.
 __host__ __device__ constexpr int merge_prefetch(int G, int D, int max_threads) {
     const int per_part = G * (D / 32);
-    const int k = (max_threads <= 32 * 12 ? 48 : 16) / per_part;
+    const int k = (max_threads <= 32 * 12 ? 32 : 16) / per_part;
     return k < 1 ? 1 : (k > 4 ? 4 : k);
 }
 
@@ -496,9 +534,12 @@ __device__ void merge_if_last(const DecodeArgs& a, int s, int h, int hw, int pai
     // Which warp merges depends on timing, so the choice of path depends on
     // the pair only; the ring (when free) changes where the loads come from,
     // not the arithmetic.
+    // (One slot a lane covers the usual split over a few CTAs; four, up to
+    // 128/G parts, a small batch spread over many.)
     if (W >= a.num_ctas && nparts * G <= 32)
-        merge_parts_small<G, D, kPre>(a, s, h, hw, pair, ca, nparts,
-                                      nparts * G * D <= scratch_floats ? scratch : nullptr);
+        merge_parts_small<G, D, kPre, 1>(a, s, h, hw, pair, ca, nparts, scratch, scratch_floats / (G * D));
+    else if (W >= a.num_ctas && nparts * G <= 128)
+        merge_parts_small<G, D, kPre, 4>(a, s, h, hw, pair, ca, nparts, scratch, scratch_floats / (G * D));
     else
         merge_parts<G, D, kPre>(a, s, h, hw, pair, ca, cb, W);
     __syncwarp();
