@@ -207,6 +207,40 @@ def test_split_merge_is_bitwise_reproducible(num_ctas):
     assert pkv.device_status() == (0, 0)
 
 
+MANY_PARTS = [  # (query heads, KV heads, head_dim, dtype, contexts, CTAs): sequences over 10-50 CTAs
+    (8, 1, 128, "bf16", (3000, 2000, 700, 1), 24),
+    (8, 4, 128, "bf16", (4000, 900), 40),
+    (4, 4, 64, "f16", (5000, 1500, 33), 64),
+]
+
+
+@pytest.mark.parametrize("shape", MANY_PARTS, ids=["G8", "G2", "G1"])
+@pytest.mark.parametrize("warps", [0, 1])
+def test_merge_of_many_parts(shape, warps):
+    """Sequences split over more than 32/G CTAs take the merge with four
+    (max, sum) slots a lane; with one warp per KV head (warps=1 a head) the
+    parts are staged through the ring in chunks.  Against the oracle, and
+    bit for bit the same over repeated calls."""
+    hq, hkv, d, dtype, ctx, ctas = shape
+    spec = small_spec(f"many{hq}_{hkv}", num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=16,
+                      dtype=dtype, seed=31 + hq + hkv, ctx=ctx)
+    pl = make_placement(spec)
+    case = SmallCase(spec, pl)
+    _, _, _, ref = case.oracle()
+    d_ = case.device()
+    slots = pkv.slot_mapping(d_["tables"], d_["ctx"], spec.block_size, pl.num_blocks)
+    d_["pool"].append(0, d_["kn"], d_["vn"], slots, seq_ids=d_["seq_ids"])
+    opts = dict(num_ctas=ctas, kernel="mma")
+    if warps:
+        opts["consumer_warps"] = hkv if hkv <= 8 else 8
+    outs = [attend(d_["q"], d_["kc"], d_["vc"], d_["tables"], d_["ctx"], spec.attn_scale,
+                   out_dtype=torch.float32, **opts) for _ in range(3)]
+    check_output(outs[0], ref, f"{shape} warps={warps}")
+    for o in outs[1:]:
+        assert torch.equal(bits(o), bits(outs[0]))
+    assert pkv.device_status() == (0, 0)
+
+
 @pytest.mark.parametrize("kernel", ["mma", "ffma"])
 def test_block_relabelling_is_bitwise_invariant(kernel):
     spec = small_spec("relabel", num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
