@@ -45,6 +45,13 @@ namespace pkv {
 // kMaxT: the largest block the instantiation is launched with.  The usual
 // launch (1 + 8 warps) takes the 384-thread variant, whose register budget
 // (168 per thread) holds the state without spilling.
+// f16x2 of p's f16 high part (low half) and the f16 rounding of the rest.
+__device__ __forceinline__ uint32_t f16_high_low(float p) {
+    const __half h = __float2half_rn(p);
+    const __half2 hl = __halves2half2(h, __float2half_rn(p - __half2float(h)));
+    return *reinterpret_cast<const uint32_t*>(&hl);
+}
+
 template <int QT, int D, bool kQ8 = false, int kMaxT = 32 * 16>
 struct MmaFp8Policy {
     static constexpr int kMaxThreads = kMaxT;
@@ -66,18 +73,20 @@ struct MmaFp8Policy {
         // f16 B fragments of Q^T, head lane/4: dims 16ks + 4(lane%4) + {0,1} / {2,3};
         // kQ8: E4M3 B fragments, dims 32j + 4(lane%4) + {0..3} / 16 + ...
         uint32_t qb[kQ8 ? K8 : KS][2];
-        float sc[2];         // kQ8: score multipliers of columns 2(lane%4), 2(lane%4)+1
+        float sc[2];         // kQ8: score multipliers of columns 2(lane%4), 2(lane%4)+1 (one head)
         float o[KS][4];      // O^T: dims 16mi + 2(lane/4) (+1 for [2],[3]), heads 2(lane%4) (+1 for [1],[3])
-        float m[2];          // running max of heads 2(lane%4), 2(lane%4)+1
-        float l[2];          // this lane's share of the running sum
+        float m[2];          // running max of heads 2(lane%4), 2(lane%4)+1 (kQ8: [0], head lane%4)
+        float l[2];          // this lane's share of the running sum (kQ8: [0])
     };
 
     // kQ8 begin: B fragments of q's two E4M3 parts and the per-column score scale.
     __device__ __forceinline__ void begin_q8(State& st, const DecodeArgs& a, int s, int h, int G) {
         const int lane = threadIdx.x & 31;
         const int g = lane >> 2, c = lane & 3;
+        // Column g carries head g/2 (repeated past G): its high part in even
+        // columns, its low part in odd ones.
         const T* q = static_cast<const T*>(a.q) +
-                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + g % G) * D;
+                     (static_cast<int64_t>(s) * a.num_q_heads + h * G + (g >> 1) % G) * D;
         float v[K8][8];
         float mx = 0.f;
 #pragma unroll
@@ -100,7 +109,7 @@ struct MmaFp8Policy {
         if (mx > 0.f) kq = 7 - (((__float_as_int(mx) >> 23) & 0xff) - 127);
         kq = kq < -120 ? -120 : (kq > 120 ? 120 : kq);
         const float up = __int_as_float((127 + kq) << 23);
-        const bool lo_part = g >= 4;
+        const bool lo_part = (g & 1) != 0;
 #pragma unroll
         for (int j = 0; j < K8; ++j) {
             uint32_t w[2];
@@ -121,8 +130,9 @@ struct MmaFp8Policy {
             st.qb[j][0] = w[0];
             st.qb[j][1] = w[1];
         }
-        const int k0 = __shfl_sync(0xffffffffu, kq, 8 * c);      // column 2c's head sits in lane 4 * 2c
-        const int k1 = __shfl_sync(0xffffffffu, kq, 8 * c + 4);  // column 2c+1
+        // Columns 2c and 2c+1 (this lane's) are both head c: rows g = 2c, 2c+1.
+        const int k0 = __shfl_sync(0xffffffffu, kq, 8 * c);
+        const int k1 = __shfl_sync(0xffffffffu, kq, 8 * c + 4);
         st.sc[0] = a.scale_log2 * __int_as_float((127 - k0) << 23);
         st.sc[1] = a.scale_log2 * __int_as_float((127 - k1) << 23);
     }
@@ -213,13 +223,50 @@ struct MmaFp8Policy {
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[n][r] = part[0][r] + part[1][r];
-            if constexpr (kQ8) {  // hi (columns < 4) + lo (columns >= 4) of the same head
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[n][r] += __shfl_xor_sync(0xffffffffu, acc[n][r], 2);
+            if constexpr (kQ8) {  // head c: its high (column 2c) and low (2c+1) parts
+                acc[n][0] += acc[n][1];
+                acc[n][2] += acc[n][3];
             }
         }
-        const float sl0 = kQ8 ? st.sc[0] : a.scale_log2 * kKUnscale;
-        const float sl1 = kQ8 ? st.sc[1] : a.scale_log2 * kKUnscale;
+        uint32_t bh[NS][2], bl[NS][2];
+        const bool packed = kQ8 || G <= 4;
+        if constexpr (kQ8) {
+            // ---- online softmax over all NS slices (head c; tokens g, g+8 of each)
+            const float sl = st.sc[0];
+            float x[NS][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < NS; ++n) {
+                const int t0 = lane >> 2;
+                x[n][0] = t0 < nv[n] ? acc[n][0] * sl : -INFINITY;
+                x[n][1] = t0 + 8 < nv[n] ? acc[n][2] * sl : -INFINITY;
+                mx = fmaxf(mx, fmaxf(x[n][0], x[n][1]));
+            }
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float mn = fmaxf(st.m[0], mx);
+            const float al = fast_exp2(st.m[0] - mn);
+            st.m[0] = mn;
+            float ls = 0.f;
+#pragma unroll
+            for (int n = 0; n < NS; ++n) {
+                const float p0 = fast_exp2(x[n][0] - mn), p1 = fast_exp2(x[n][1] - mn);
+                ls += p0 + p1;
+                // P^T fragments: column 2c the f16 high part of head c's p, 2c+1 the low part.
+                bh[n][0] = movmatrix_trans(f16_high_low(p0));
+                bh[n][1] = movmatrix_trans(f16_high_low(p1));
+                bl[n][0] = bl[n][1] = 0u;
+            }
+            st.l[0] = st.l[0] * al + ls;
+            if (__any_sync(0xffffffffu, al != 1.f)) {
+#pragma unroll
+                for (int mi = 0; mi < KS; ++mi)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) st.o[mi][r] *= al;
+            }
+        } else {
+        const float sl0 = a.scale_log2 * kKUnscale;
+        const float sl1 = a.scale_log2 * kKUnscale;
         // ---- online softmax over all NS slices (heads 2c, 2c+1; tokens g, g+8 of each)
         float x[NS][4];
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -244,8 +291,6 @@ struct MmaFp8Policy {
         st.m[0] = mn0;
         st.m[1] = mn1;
         float ls0 = 0.f, ls1 = 0.f;
-        uint32_t bh[NS][2], bl[NS][2];
-        const bool packed = kQ8 || G <= 4;
         const bool lo_cols = (lane & 3) >= 2;
 #pragma unroll
         for (int n = 0; n < NS; ++n) {
@@ -276,6 +321,7 @@ struct MmaFp8Policy {
                 st.o[mi][2] *= al0;
                 st.o[mi][3] *= al1;
             }
+        }
         }
         // ---- O^T += V^T . P^T
 #pragma unroll
@@ -376,6 +422,23 @@ struct MmaFp8Policy {
                                          int G) const {
         const int lane = threadIdx.x & 31;
         const int g = lane >> 2, c = lane & 3;
+        if constexpr (kQ8) {  // head c: its high and low columns summed
+            float l = st.l[0];
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (c >= G) return;
+#pragma unroll
+            for (int mi = 0; mi < KS; ++mi) {
+                const int d0 = 16 * mi + 2 * g;
+                o[c * os + d0] = (st.o[mi][0] + st.o[mi][1]) * vs;
+                o[c * os + d0 + 1] = (st.o[mi][2] + st.o[mi][3]) * vs;
+            }
+            if (g == 0) {
+                ml[c * ms] = st.m[0];
+                ml[c * ms + 1] = l;
+            }
+            return;
+        }
         float l0, l1;
         row_sums(st, l0, l1);
         const int h0 = 2 * c, h1 = 2 * c + 1;
@@ -420,6 +483,21 @@ struct MmaFp8Policy {
                                                 int G) const {
         const int lane = threadIdx.x & 31;
         const int g = lane >> 2, c = lane & 3;
+        if constexpr (kQ8) {  // head c: its high and low columns summed
+            float l = st.l[0];
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (c >= G) return;
+            const float inv = a.v_scale * kVUnscale / l;
+            const int64_t base = (static_cast<int64_t>(s) * a.num_q_heads + h * G + c) * D;
+#pragma unroll
+            for (int mi = 0; mi < KS; ++mi) {
+                const int d0 = 16 * mi + 2 * g;
+                store_out(a.out, base + d0, (st.o[mi][0] + st.o[mi][1]) * inv, a.out_dtype);
+                store_out(a.out, base + d0 + 1, (st.o[mi][2] + st.o[mi][3]) * inv, a.out_dtype);
+            }
+            return;
+        }
         float l0, l1;
         row_sums(st, l0, l1);
         const float i0 = a.v_scale * kVUnscale / l0, i1 = a.v_scale * kVUnscale / l1;
