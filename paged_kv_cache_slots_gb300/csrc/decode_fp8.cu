@@ -32,19 +32,6 @@
 
 namespace pkv {
 
-// kQ8: QK on the E4M3 tensor path (bf16 q, at most 4 query heads per KV
-// head).  The K tile feeds the m16n8k32 E4M3 MMA straight from ldmatrix (a
-// lane's four consecutive codes are exactly its A-fragment bytes), so K needs
-// no conversion.  q is scaled per head by a power of two 2^kq (largest |q| to
-// [128, 256)) and split exactly into two E4M3 parts, hi = RN(q') and
-// lo = q' - hi (a bf16 value has 8 significant bits, each part holds 4, and
-// the rounding residual of hi is a multiple of hi's last-bit weight / 16 no
-// larger than half of it, so it fits 4 bits): columns 0-3 carry hi and
-// columns 4-7 lo of heads col % G, and the two halves of each score are
-// added with one shuffle.  Scores then carry scale * log2(e) * k_scale * 2^-kq.
-// kMaxT: the largest block the instantiation is launched with.  The usual
-// launch (1 + 8 warps) takes the 384-thread variant, whose register budget
-// (168 per thread) holds the state without spilling.
 // f16x2 of p's f16 high part (low half) and the f16 rounding of the rest.
 __device__ __forceinline__ uint32_t f16_high_low(float p) {
     const __half h = __float2half_rn(p);
@@ -52,6 +39,21 @@ __device__ __forceinline__ uint32_t f16_high_low(float p) {
     return *reinterpret_cast<const uint32_t*>(&hl);
 }
 
+// kQ8: QK on the E4M3 tensor path (bf16 q, at most 4 query heads per KV
+// head).  The K tile feeds the m16n8k32 E4M3 MMA straight from ldmatrix (a
+// lane's four consecutive codes are exactly its A-fragment bytes), so K needs
+// no conversion.  q is scaled per head by a power of two 2^kq (largest |q| to
+// [128, 256)) and split exactly into two E4M3 parts, hi = RN(q') and
+// lo = q' - hi (a bf16 value has 8 significant bits, each part holds 4, and
+// the rounding residual of hi is a multiple of hi's last-bit weight / 16 no
+// larger than half of it, so it fits 4 bits): column 2j carries hi and column
+// 2j+1 lo of head j (heads past G repeat), so lane c's two accumulator columns
+// are head c's two halves, added in place; the softmax, P's fragments and the
+// output then take one head a lane.  Scores carry
+// scale * log2(e) * k_scale * 2^-kq.
+// kMaxT: the largest block the instantiation is launched with.  The usual
+// launch (1 + 8 warps) takes the 384-thread variant, whose register budget
+// (168 per thread) holds the state without spilling.
 template <int QT, int D, bool kQ8 = false, int kMaxT = 32 * 16>
 struct MmaFp8Policy {
     static constexpr int kMaxThreads = kMaxT;
