@@ -63,7 +63,11 @@ extern "C" {
  * type of KV pools only ("vLLM Architecture and Installation", Example 6:
  * an FP8 KV cache takes one byte per value).  A code b of a layer's K (V)
  * stands for k_scale (v_scale) * e4m3(b); the scales are fp32, one per layer
- * for K and one for V, owned by the caller and passed to every call. */
+ * for K and one for V, owned by the caller and passed to every call.  The
+ * library's quantizer never writes the NaN codes (it saturates at 448); NaN
+ * codes written into a pool by other code are not guaranteed to propagate:
+ * where the attention kernels convert codes with integer operations (V
+ * always, K with an f16 q or 8 query heads per KV head) they read as +-480. */
 typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2, KV_FP8_E4M3 = 3 } kv_dtype_t;
 
 typedef enum {
@@ -280,8 +284,11 @@ kv_status_t paged_decode_append_attention(const void* q, const void* k_new, cons
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   The first call on a device takes the array's device address (and may
  *   load the library's device code there): make it before any stream capture.
- *   Each call clears the array's merge counters on `stream` first.  All calls
- *   on a device share the array: calls that overlap on the GPU race.
+ *   The address is kept for the life of the process, so the library must not
+ *   be called on a device after cudaDeviceReset there.
+ *   Each accepted call clears the array's merge counters on `stream` right
+ *   before its kernel; a refused call (any error status) queues nothing.
+ *   All calls on a device share the array: calls that overlap on the GPU race.
  * The other arguments and the result are those of paged_decode_attention. */
 kv_status_t paged_decode_attention_static(const void* q, const void* k_cache, const void* v_cache,
                                           int num_blocks, const int32_t* block_tables,

@@ -155,6 +155,17 @@ def _stream(t: torch.Tensor, stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _call_on(t: torch.Tensor, lib, fn, *args):
+    """Call a library entry point with t's device current: the library takes
+    the SM count, the status word and the static scratch of the current
+    device, and the stream passed is t's."""
+    if t.device.type != "cuda":  # the library rejects host pointers where it needs device memory
+        _check(fn(*args), lib)
+        return
+    with torch.cuda.device(t.device):
+        _check(fn(*args), lib)
+
+
 def _need(cond: bool, msg: str):
     if not cond:
         raise ValueError(msg)
@@ -322,8 +333,9 @@ def slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor, block_s
     _need(block_tables.is_contiguous() and block_tables.shape[0] == B, "block_tables [B, max_blocks]")
     if out is None:
         out = torch.empty(B, dtype=torch.int32, device=context_lens.device)
-    _check(lib.kv_slot_mapping(_ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
-                               block_size, num_blocks, _ptr(out), _stream(out, stream)), lib)
+    _call_on(context_lens, lib, lib.kv_slot_mapping,
+             _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
+             block_size, num_blocks, _ptr(out), _stream(out, stream))
     return out
 
 
@@ -336,8 +348,9 @@ def _options(num_ctas=0, ctas_per_sm=0, consumer_warps=0, kernel="auto", heads_p
 def workspace_init(workspace: torch.Tensor, num_seqs: int, num_kv_heads: int, stream=None):
     """Zero the merge counters at the start of a workspace (once after allocation)."""
     lib = load_library()
-    _check(lib.paged_decode_workspace_init(_ptr(workspace), workspace.numel(), num_seqs, num_kv_heads,
-                                           _stream(workspace, stream)), lib)
+    _call_on(workspace, lib, lib.paged_decode_workspace_init,
+             _ptr(workspace), workspace.numel(), num_seqs, num_kv_heads,
+                                           _stream(workspace, stream))
 
 
 def make_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, device=None, **opts) -> torch.Tensor:
@@ -389,17 +402,17 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     if workspace is None:
         workspace = make_workspace(B, Hq, Hkv, D, q.device, **opts)
     if fp8:
-        _check(lib.paged_decode_attention_fp8(
+        _call_on(q, lib, lib.paged_decode_attention_fp8,
             _ptr(q), DTYPE_CODE[q.dtype], _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale),
             NB, _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
             float(scale), _ptr(out), DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(),
-            ctypes.byref(o), _stream(q, stream)), lib)
+            ctypes.byref(o), _stream(q, stream))
         return out
-    _check(lib.paged_decode_attention(
+    _call_on(q, lib, lib.paged_decode_attention,
         _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), B, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale), _ptr(out),
         DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(), ctypes.byref(o),
-        _stream(q, stream)), lib)
+        _stream(q, stream))
     return out
 
 
@@ -440,18 +453,18 @@ def paged_decode_append_attention(q, k_new, v_new, k_cache, v_cache, block_table
     if workspace is None:
         workspace = make_workspace(B, Hq, Hkv, D, q.device, **opts)
     if fp8:
-        _check(lib.paged_decode_append_attention_fp8(
+        _call_on(q, lib, lib.paged_decode_append_attention_fp8,
             _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_ids), DTYPE_CODE[q.dtype], _ptr(k_cache),
             _ptr(v_cache), float(k_scale), float(v_scale), NB, _ptr(block_tables), block_tables.shape[1],
             _ptr(context_lens), B, Hq, Hkv, D, bs, float(scale), _ptr(out), DTYPE_CODE[out_dtype],
             _ptr(slot_mapping), _ptr(workspace), workspace.numel(), ctypes.byref(o),
-            _stream(q, stream)), lib)
+            _stream(q, stream))
         return out
-    _check(lib.paged_decode_append_attention(
+    _call_on(q, lib, lib.paged_decode_append_attention,
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(seq_ids), _ptr(k_cache), _ptr(v_cache), NB,
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
         DTYPE_CODE[q.dtype], float(scale), _ptr(out), DTYPE_CODE[out_dtype], _ptr(slot_mapping),
-        _ptr(workspace), workspace.numel(), ctypes.byref(o), _stream(q, stream)), lib)
+        _ptr(workspace), workspace.numel(), ctypes.byref(o), _stream(q, stream))
     return out
 
 
@@ -469,9 +482,10 @@ def slot_mapping_varlen(block_tables: torch.Tensor, query_start: torch.Tensor, c
         num_tokens = int(query_start[-1].item())
     if out is None:
         out = torch.empty(max(num_tokens, 1), dtype=torch.int32, device=context_lens.device)[:num_tokens]
-    _check(lib.kv_slot_mapping_varlen(_ptr(block_tables), block_tables.shape[1], _ptr(query_start),
-                                      _ptr(context_lens), B, num_tokens, block_size, num_blocks, _ptr(out),
-                                      _stream(context_lens, stream)), lib)
+    _call_on(context_lens, lib, lib.kv_slot_mapping_varlen,
+             _ptr(block_tables), block_tables.shape[1], _ptr(query_start),
+             _ptr(context_lens), B, num_tokens, block_size, num_blocks, _ptr(out),
+             _stream(context_lens, stream))
     return out
 
 
@@ -497,10 +511,10 @@ def paged_prefill_attention(q, k_cache, v_cache, block_tables, query_start, cont
     if workspace is None:
         workspace = torch.empty(max(16, int(lib.paged_prefill_workspace_bytes(B))), dtype=torch.uint8,
                                 device=q.device)
-    _check(lib.paged_prefill_attention(
+    _call_on(q, lib, lib.paged_prefill_attention,
         _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
         _ptr(query_start), _ptr(context_lens), B, T, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale),
-        _ptr(out), DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(), _stream(q, stream)), lib)
+        _ptr(out), DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(), _stream(q, stream))
     return out
 
 
@@ -520,10 +534,10 @@ def paged_decode_attention_static(q, k_cache, v_cache, block_tables, context_len
     _need(out is not None, "out must be given (the call allocates nothing)")
     _need(out.dtype == out_dtype and tuple(out.shape) == (B, Hq, D) and out.is_contiguous(), "out")
     o = _options(**opts)
-    _check(lib.paged_decode_attention_static(
+    _call_on(q, lib, lib.paged_decode_attention_static,
         _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), B, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale), _ptr(out),
-        DTYPE_CODE[out_dtype], ctypes.byref(o), _stream(q, stream)), lib)
+        DTYPE_CODE[out_dtype], ctypes.byref(o), _stream(q, stream))
     return out
 
 

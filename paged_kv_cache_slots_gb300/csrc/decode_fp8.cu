@@ -17,14 +17,16 @@
 //    dims 16j + 4c .. 16j + 4c + 3 of a 16-dim chunk j (c = lane % 4).  The
 //    dot product does not care in which order dims are summed, so the MMA's
 //    k index is permuted inside each chunk: logical columns 2c, 2c+1 hold
-//    dims 4c, 4c+1 and logical columns 2c+8, 2c+9 hold dims 4c+2, 4c+3, and
-//    the q fragments are built with the same permutation.  One ldmatrix.x4
-//    then yields the A fragments of two 16-dim chunks.
+//    dims 4c, 4c+2 (the word's even bytes) and logical columns 2c+8, 2c+9
+//    hold dims 4c+1, 4c+3 (its odd bytes), and the q fragments are built
+//    with the same permutation.  One ldmatrix.x4 then yields the A fragments
+//    of two 16-dim chunks.
 //  - V (transposed): a lane receives the code pairs (2g, 2g+1) of tokens 2c
-//    and 2c+1 (g = lane / 4); a byte permute regroups them into the token
-//    pairs of dim 2g and of dim 2g+1.  So M row g of a 16-dim chunk is dim
-//    2g and row g+8 is dim 2g+1, and the output accumulators are written
-//    back with that mapping.
+//    and 2c+1 (g = lane / 4): the word's even bytes are the token pair of
+//    dim 2g and its odd bytes that of dim 2g+1, each converted in place (no
+//    byte permute).  So M row g of a 16-dim chunk is dim 2g and row g+8 is
+//    dim 2g+1, and the output accumulators are written back with that
+//    mapping.
 // Tiles arrive through 2-D tensor maps with a 128-byte swizzle: rows of 128
 // codes (head_dim 128), chunk c of row r stored at chunk c ^ (r % 8).
 #include "decode_kernel.cuh"
@@ -65,7 +67,7 @@ struct MmaFp8Policy {
     static constexpr int K8 = D / 32;  // 32-dim k-slices of the E4M3 QK
     static constexpr int kD = D;
     // V enters the P.V product as its E4M3 value times 2^-8 (see
-    // e4m3x2_to_half2_shifted); the outputs are scaled back by 2^8, exactly.
+    // e4m3x2_odd_bytes_to_half2_shifted); the outputs are scaled back by 2^8, exactly.
     static constexpr float kVUnscale = 256.f;
     // Likewise K in the f16 form of Q.K^T (not kQ8, where the MMA takes the codes).
     static constexpr float kKUnscale = 256.f;
@@ -158,14 +160,15 @@ struct MmaFp8Policy {
                      (static_cast<int64_t>(s) * a.num_q_heads + h * G + g % G) * D;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
+            // Dims 4c, 4c+2 (k = 2c, 2c+1) and 4c+1, 4c+3 (k = 2c+8, 2c+9), as K's fragments.
             const uint2 raw = *reinterpret_cast<const uint2*>(q + 16 * ks + 4 * c);
             if constexpr (QT == kF16) {
-                st.qb[ks][0] = raw.x;
-                st.qb[ks][1] = raw.y;
+                st.qb[ks][0] = __byte_perm(raw.x, raw.y, 0x5410u);
+                st.qb[ks][1] = __byte_perm(raw.x, raw.y, 0x7632u);
             } else {
                 const T* e = reinterpret_cast<const T*>(&raw);
-                const __half2 h0 = __floats2half2_rn(Elem<QT>::to_float(e[0]), Elem<QT>::to_float(e[1]));
-                const __half2 h1 = __floats2half2_rn(Elem<QT>::to_float(e[2]), Elem<QT>::to_float(e[3]));
+                const __half2 h0 = __floats2half2_rn(Elem<QT>::to_float(e[0]), Elem<QT>::to_float(e[2]));
+                const __half2 h1 = __floats2half2_rn(Elem<QT>::to_float(e[1]), Elem<QT>::to_float(e[3]));
                 st.qb[ks][0] = *reinterpret_cast<const uint32_t*>(&h0);
                 st.qb[ks][1] = *reinterpret_cast<const uint32_t*>(&h1);
             }
@@ -214,11 +217,12 @@ struct MmaFp8Policy {
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {  // chunk 2kp + hf: rows g / g+8 in r[2hf] / r[2hf+1]
                         uint32_t af[4];
-                        // K codes as f16 values times 2^-8 (kKUnscale restores the scores)
-                        af[0] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4140u));
-                        af[1] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4140u));
-                        af[2] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4342u));
-                        af[3] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4342u));
+                        // K codes as f16 values times 2^-8 (kKUnscale restores the scores):
+                        // even bytes are k = 2c, 2c+1, odd bytes k = 2c+8, 2c+9.
+                        af[0] = e4m3x2_even_bytes_to_half2_shifted(r[2 * hf]);
+                        af[1] = e4m3x2_even_bytes_to_half2_shifted(r[2 * hf + 1]);
+                        af[2] = e4m3x2_odd_bytes_to_half2_shifted(r[2 * hf]);
+                        af[3] = e4m3x2_odd_bytes_to_half2_shifted(r[2 * hf + 1]);
                         mma16816<kF16>(part[hf], af, st.qb[2 * kp + hf][0], st.qb[2 * kp + hf][1]);
                     }
                 }
@@ -337,10 +341,10 @@ struct MmaFp8Policy {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t af[4];
-                    af[0] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4240u));      // dim 2g,   tokens 2c, 2c+1
-                    af[1] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf], 0u, 0x4341u));      // dim 2g+1, tokens 2c, 2c+1
-                    af[2] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4240u));  // dim 2g,   tokens 8+2c, 9+2c
-                    af[3] = e4m3x2_to_half2_shifted(__byte_perm(r[2 * hf + 1], 0u, 0x4341u));  // dim 2g+1, tokens 8+2c, 9+2c
+                    af[0] = e4m3x2_even_bytes_to_half2_shifted(r[2 * hf]);     // dim 2g,   tokens 2c, 2c+1
+                    af[1] = e4m3x2_odd_bytes_to_half2_shifted(r[2 * hf]);      // dim 2g+1, tokens 2c, 2c+1
+                    af[2] = e4m3x2_even_bytes_to_half2_shifted(r[2 * hf + 1]); // dim 2g,   tokens 8+2c, 9+2c
+                    af[3] = e4m3x2_odd_bytes_to_half2_shifted(r[2 * hf + 1]);  // dim 2g+1, tokens 8+2c, 9+2c
                     mma16816<kF16>(st.o[2 * mp + hf], af, bh[n][0], bh[n][1]);
                     if (!packed) mma16816<kF16>(st.o[2 * mp + hf], af, bl[n][0], bl[n][1]);
                 }

@@ -17,15 +17,22 @@
 // it before capturing a stream into a CUDA graph.
 //
 // Every call shares the one array per device and the array keeps the last
-// call's contents: each call clears the part that must start at zero (the
-// merge counters) on its stream before the kernel runs.  Two calls that
-// overlap on the GPU (different streams, no ordering between them) race on
-// the array and give undefined results.
+// call's contents: each accepted call clears the part that must start at
+// zero (the merge counters) on its stream right before the kernel runs; a
+// call that is refused queues nothing.  Two calls that overlap on the GPU
+// (different streams, no ordering between them) race on the array and give
+// undefined results.
+//
+// The device address is cached for the life of the process.  After
+// cudaDeviceReset the device's module is loaded afresh and the cached
+// address is stale: a process that resets a device must not call the
+// library on it again (the status word's address is cached the same way).
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "pkv.h"
+#include "pkv_internal.h"
 
 namespace {
 
@@ -64,23 +71,23 @@ extern "C" kv_status_t paged_decode_attention_static(
     if (device < 0 || device >= kMaxDevices) return KV_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     if (scratch_address(device, &scratch) != cudaSuccess) return KV_ERR_CUDA;
+    // Sizes that need more scratch than the array holds are refused here,
+    // before anything is queued, with both sizes in kv_last_error().
     if (num_seqs > 0 && num_kv_heads > 0 && num_q_heads > 0 && head_dim > 0 &&
         num_q_heads % num_kv_heads == 0) {
         size_t need = 0;
         const kv_status_t st = paged_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
                                                             head_dim, device, opts, &need);
         if (st != KV_OK) return st;
-        // Within the array: clear the merge counters.  Beyond it: the call
-        // below rejects the sizes before launching anything, returns
-        // KV_ERR_WORKSPACE_TOO_SMALL and names both sizes in kv_last_error().
-        if (need <= kStaticScratchBytes) {
-            const kv_status_t zs = paged_decode_workspace_init(scratch, kStaticScratchBytes, num_seqs,
-                                                               num_kv_heads, stream);
-            if (zs != KV_OK) return zs;
-        }
+        if (need > kStaticScratchBytes)
+            return pkv::report_error(KV_ERR_WORKSPACE_TOO_SMALL,
+                                     "static scratch workspace holds %zu bytes, these sizes need %zu",
+                                     kStaticScratchBytes, need);
     }
-    return paged_decode_attention(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_seq,
-                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                  block_size, dtype, scale, out, out_dtype, scratch,
-                                  kStaticScratchBytes, opts, stream);
+    // Every other check runs inside; the merge counters are zeroed on
+    // `stream` only once the call is accepted, right before its launch.
+    return pkv::decode_attention_clearing_counters(q, k_cache, v_cache, num_blocks, block_tables,
+                                                   max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                                                   num_kv_heads, head_dim, block_size, dtype, scale, out,
+                                                   out_dtype, scratch, kStaticScratchBytes, opts, stream);
 }

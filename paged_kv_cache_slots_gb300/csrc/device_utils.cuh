@@ -255,14 +255,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t v) {
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
-// Two E4M3 codes in bytes 0 and 2 of y (bytes 1 and 3 zero) -> f16x2 of
-// their values times 2^-8, exactly, in integer operations: an E4M3 code
+// E4M3 -> f16 in integer operations, exactly, times 2^-8: an E4M3 code
 // s.eeee.mmm read as the f16 bit pattern s.0eeee.mmm0000000 has exponent
 // field eeee, i.e. the same value scaled by 2^(7 - 15), subnormals included.
-// The magnitude moves up 7 bits and the sign 8: (y + (y & 0x80)) << 7 does
-// both in each 16-bit half without carries between the halves.
-__device__ __forceinline__ uint32_t e4m3x2_to_half2_shifted(uint32_t y) {
-    return (y + (y & 0x00800080u)) << 7;
+// Two codes of a 32-bit word are converted at once, each into one 16-bit
+// half of the result.
+//
+// Codes in bytes 1 and 3 of r (bytes 0 and 2 ignored): each code's sign
+// already sits at bit 15 of its half, and its seven magnitude bits move down
+// one place to bits 13..7 -- one shift and one three-input logic operation.
+__device__ __forceinline__ uint32_t e4m3x2_odd_bytes_to_half2_shifted(uint32_t r) {
+    return ((r >> 1) & 0x3F803F80u) | (r & 0x80008000u);
+}
+
+// Codes in bytes 0 and 2 of r (bytes 1 and 3 ignored): moved up one byte
+// first, then as above.
+__device__ __forceinline__ uint32_t e4m3x2_even_bytes_to_half2_shifted(uint32_t r) {
+    return e4m3x2_odd_bytes_to_half2_shifted(r << 8);
 }
 
 // Store an fp32 value as out_dtype (round to nearest even).

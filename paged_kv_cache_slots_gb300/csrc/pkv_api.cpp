@@ -504,7 +504,8 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
                                kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
                                const kv_decode_options_t* opts, void* stream, const void* k_new,
                                const void* v_new, const int32_t* append_ids, int32_t* slot_out,
-                               kv_dtype_t kv_dtype, float k_scale, float v_scale) {
+                               kv_dtype_t kv_dtype, float k_scale, float v_scale,
+                               bool clear_counters = false) {
     const bool fp8 = kv_dtype == KV_FP8_E4M3;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
         return fail(KV_ERR_INVALID_ARG, "paged_decode_attention: sizes out of range");
@@ -638,11 +639,17 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    CUtensorMap tk, tv;
     if (kernel == KV_KERNEL_MMA) {
-        CUtensorMap tk, tv;
         const int rows = num_blocks * num_kv_heads * block_size;
         if (kv_status_t st = encode_cache_map(&tk, k_cache, kv_dtype, rows, head_dim, hc * block_size)) return st;
         if (kv_status_t st = encode_cache_map(&tv, v_cache, kv_dtype, rows, head_dim, hc * block_size)) return st;
+    }
+    if (clear_counters) {
+        e = cudaMemsetAsync(ws + wl.counters, 0, static_cast<size_t>(num_seqs) * num_kv_heads * 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (kernel == KV_KERNEL_MMA) {
         e = fp8 ? launch_decode_fp8(a, tk, tv, s) : launch_decode_mma(a, tk, tv, s);
     } else {
         e = launch_decode_ffma(a, s);
@@ -967,3 +974,19 @@ kv_status_t kv_allocator_free_queue(const kv_block_allocator_t* a, int32_t* out,
 }
 
 }  // extern "C"
+
+namespace pkv {
+kv_status_t decode_attention_clearing_counters(const void* q, const void* k_cache, const void* v_cache,
+                                               int num_blocks, const int32_t* block_tables, int max_blocks,
+                                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                               int num_kv_heads, int head_dim, int block_size, int dtype,
+                                               float scale, void* out, int out_dtype, void* workspace,
+                                               size_t workspace_bytes, const void* opts, void* stream) {
+    const kv_dtype_t dt = static_cast<kv_dtype_t>(dtype);
+    return decode_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, dt, scale, out,
+                       static_cast<kv_dtype_t>(out_dtype), workspace, workspace_bytes,
+                       static_cast<const kv_decode_options_t*>(opts), stream, nullptr, nullptr, nullptr,
+                       nullptr, dt, 1.f, 1.f, /*clear_counters=*/true);
+}
+}  // namespace pkv

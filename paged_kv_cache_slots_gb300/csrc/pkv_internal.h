@@ -151,6 +151,16 @@ int max_dynamic_smem(int device);
 // Device address of the current device's status word.
 cudaError_t status_word_address(uint32_t** ptr);
 
+// paged_decode_attention that zeroes the workspace's merge counters on
+// `stream` once every argument has been checked and the launch is planned,
+// right before the launch; a call that is rejected touches nothing.
+kv_status_t decode_attention_clearing_counters(const void* q, const void* k_cache, const void* v_cache,
+                                               int num_blocks, const int32_t* block_tables, int max_blocks,
+                                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                               int num_kv_heads, int head_dim, int block_size, int dtype,
+                                               float scale, void* out, int out_dtype, void* workspace,
+                                               size_t workspace_bytes, const void* opts, void* stream);
+
 // Records a printf-style message for kv_last_error() on this thread and
 // returns st.
 kv_status_t report_error(kv_status_t st, const char* fmt, ...);

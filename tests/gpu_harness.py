@@ -41,6 +41,28 @@ def check_output(out: torch.Tensor, ref: np.ndarray, what: str):
     return float(err.max()) if err.size else 0.0
 
 
+def ordered_bits(t: torch.Tensor) -> torch.Tensor:
+    """Bit patterns of a 16- or 32-bit float tensor mapped to integers that
+    increase with the value (so that two values' distance in ulps is the
+    difference of their images); -0 and +0 map to 0."""
+    b = bits(t).to(torch.int64)
+    width = 8 * t.element_size()
+    mag = b & ((1 << (width - 1)) - 1)
+    return torch.where(b < 0, -mag, mag)
+
+
+def check_cast(outq: torch.Tensor, out32: torch.Tensor, what: str, max_ulps: int = 1):
+    """The fp16/bf16 output is the fp32 output of the same computation rounded
+    to nearest even into that type, within `max_ulps` units in the last place
+    (the final fold of a separate call may round one fp32 ulp differently)."""
+    assert outq.dtype in (torch.float16, torch.bfloat16) and out32.dtype == torch.float32
+    ref = out32.to(outq.dtype)  # round to nearest even
+    d = (ordered_bits(outq.contiguous()) - ordered_bits(ref.contiguous())).abs()
+    worst = int(d.max().item()) if d.numel() else 0
+    assert worst <= max_ulps, f"{what}: {outq.dtype} output {worst} ulps from the rounded fp32 output"
+    return worst
+
+
 def _ws_opts(opts):
     return {k: v for k, v in opts.items() if k not in ("test_stall", "k_scale", "v_scale")}
 
@@ -176,15 +198,26 @@ class LargeCase:
         q, kn, vn = step_layer_values(self.spec, len(self.pl.context_lens), layer, self.dev)
         return kc, vc, q, kn, vn
 
-    def check_layer(self, layer, seqs, fused=False, **opts):
-        """Run one layer on the full batch; compare sampled sequences with the oracle.
+    def check_layer(self, layer, seqs=None, fused=False, whole_pool=True, **opts):
+        """Run one layer on the full batch; compare with the oracle.
 
-        fused: append and attention in one call (paged_decode_append_attention)."""
+        seqs: the sequences whose outputs are checked (None: every sequence).
+        whole_pool: bit-compare the whole layer pool after the append with the
+        oracle's scatter of every sequence's new rows into a host copy of the
+        pre-step pool (else only the blocks of `seqs`, over a compact copy).
+        fused: append and attention in one call (paged_decode_append_attention).
+        Returns (max err of the fp32 output, of the q-dtype output, fp32 output
+        on the device, q-dtype output on the device)."""
         s, pl = self.spec, self.pl
+        B = len(pl.context_lens)
+        seqs = np.arange(B) if seqs is None else np.asarray(seqs, dtype=np.int64)
         kc, vc, q, kn, vn = self.fill(layer)
-        used, ctab = compact_blocks(pl.block_tables, seqs)
-        used_t = torch.from_numpy(used.astype(np.int64)).to(self.dev)
-        k_pre, v_pre = take(kc, used_t).cpu(), take(vc, used_t).cpu()  # the oracle's pool: pre-append
+        if whole_pool:
+            k_pre, v_pre = kc.cpu(), vc.cpu()  # the oracle's pool: pre-append, every block
+        else:
+            used, ctab = compact_blocks(pl.block_tables, seqs)
+            used_t = torch.from_numpy(used.astype(np.int64)).to(self.dev)
+            k_pre, v_pre = take(kc, used_t).cpu(), take(vc, used_t).cpu()
         so = scale_opts(s)
         if fused:
             out32, slots = attend_append(q, kn, vn, kc, vc, self.tables, self.ctx, s.attn_scale,
@@ -197,23 +230,49 @@ class LargeCase:
         outq = attend(q, kc, vc, self.tables, self.ctx, s.attn_scale, **so, **opts)
         st, flags = pkv.device_status()
         assert st == 0 and flags == 0, f"device status {st} flags {flags:#x}"
-        # Oracle on the sampled sequences, over the compact pool.
         ctx_s = pl.context_lens[seqs]
-        o_sl = oracle.slot_mapping(ctab, ctx_s, s.block_size)
-        o_sl = np.where(pl.appends[seqs], o_sl, -1).astype(np.int32)
-        kn_s, vn_s, q_s = kn[seqs].cpu(), vn[seqs].cpu(), q[seqs].cpu()
-        k_post, v_post = oracle_append(s, k_pre, v_pre, kn_s, vn_s, o_sl)
-        ref = oracle_attention(s, q_s, k_post, v_post, ctab, ctx_s)
-        # Append: every sampled block bit-exact after the step.
-        assert torch.equal(cache_bits(take(kc, used_t).cpu()), cache_bits(k_post)), "K blocks after append"
-        assert torch.equal(cache_bits(take(vc, used_t).cpu()), cache_bits(v_post)), "V blocks after append"
-        # Device slot mapping: bit-exact for the sampled sequences (real table).
-        o_full = oracle.slot_mapping(pl.block_tables[seqs], ctx_s, s.block_size)
-        assert np.array_equal(slots.cpu().numpy()[seqs], o_full), "slot mapping"
+        o_full = oracle.slot_mapping(pl.block_tables, pl.context_lens, s.block_size)
+        # Device slot mapping: bit-exact for every sequence (real table).
+        assert np.array_equal(slots.cpu().numpy(), o_full), "slot mapping"
+        if whole_pool:
+            o_sl = np.where(pl.appends, o_full, -1).astype(np.int32)
+            k_post, v_post = oracle_append(s, k_pre, v_pre, kn.cpu(), vn.cpu(), o_sl)
+            assert torch.equal(cache_bits(kc.cpu()), cache_bits(k_post)), "K pool after append"
+            assert torch.equal(cache_bits(vc.cpu()), cache_bits(v_post)), "V pool after append"
+            tab = pl.block_tables[seqs]
+        else:
+            o_sl = oracle.slot_mapping(ctab, ctx_s, s.block_size)
+            o_sl = np.where(pl.appends[seqs], o_sl, -1).astype(np.int32)
+            k_post, v_post = oracle_append(s, k_pre, v_pre, kn[seqs].cpu(), vn[seqs].cpu(), o_sl)
+            assert torch.equal(cache_bits(take(kc, used_t).cpu()), cache_bits(k_post)), "K blocks after append"
+            assert torch.equal(cache_bits(take(vc, used_t).cpu()), cache_bits(v_post)), "V blocks after append"
+            tab = ctab
+        ref = oracle_attention(s, q[seqs].cpu(), k_post, v_post, tab, ctx_s)
+        del k_pre, v_pre, k_post, v_post
         idx = torch.as_tensor(seqs, device=self.dev)
         e32 = check_output(out32[idx], ref, f"{s.name} layer {layer} fp32 out")
         eq = check_output(outq[idx], ref, f"{s.name} layer {layer} {s.dtype} out")
-        return e32, eq
+        check_cast(outq, out32, f"{s.name} layer {layer}")
+        return e32, eq, out32, outq
+
+    def solo_agreement(self, layer, seqs, batch_out32, **opts):
+        """Each sequence of `seqs` attended alone (a batch of one: its table
+        row and length, the same pool) against its row of the full batch's
+        fp32 output.  Returns (max |difference|, sequences whose bits agree)."""
+        s = self.spec
+        kc, vc = self.pool.layer(layer)
+        q, _, _ = step_layer_values(s, len(self.pl.context_lens), layer, self.dev)
+        worst, same = 0.0, 0
+        for i in seqs:
+            i = int(i)
+            one = attend(q[i:i + 1].contiguous(), kc, vc, self.tables[i:i + 1].contiguous(),
+                         self.ctx[i:i + 1].contiguous(), s.attn_scale, out_dtype=torch.float32,
+                         **scale_opts(s), **opts)
+            d = (one[0] - batch_out32[i]).abs().max().item()
+            worst = max(worst, d)
+            same += int(torch.equal(bits(one[0]), bits(batch_out32[i])))
+        assert pkv.device_status() == (0, 0)
+        return worst, same
 
 
 def sample_sequences(placement, n, seed):

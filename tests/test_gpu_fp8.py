@@ -10,8 +10,8 @@ import pytest
 import torch
 
 import paged_kv_cache_slots_gb300 as pkv
-from gpu_harness import (LargeCase, SmallCase, attend, attend_append, cache_bits, check_output,
-                         run_step, sample_sequences, scale_opts)
+from gpu_harness import (LargeCase, SmallCase, attend, attend_append, cache_bits, check_cast, check_output,
+                         run_step, scale_opts)
 from workloads import SPECS, make_placement, small_spec
 
 pytestmark = pytest.mark.gpu
@@ -44,6 +44,7 @@ def _check_all(spec, placement=None, **opts):
     assert torch.equal(cache_bits(d["vc"].cpu()), cache_bits(vpost)), "V codes after append"
     e32 = check_output(out, ref, f"{spec.name} fp32 out")
     check_output(outq, ref, f"{spec.name} {spec.dtype} out")
+    check_cast(outq, out, spec.name)
     d = case.device()
     out_f, slots_f = attend_append(d["q"], d["kn"], d["vn"], d["kc"], d["vc"], d["tables"], d["ctx"],
                                    spec.attn_scale, seq_ids=d["seq_ids"], out_dtype=torch.float32,
@@ -100,12 +101,24 @@ def test_fp8_launch_shapes(opts):
     _check_all(spec, **opts)
 
 
-def test_fp8_batch32_32_layers_sampled():
+def test_fp8_batch32_32_layers_every_sequence():
+    """The E4M3 batch-32 step at full size: every sequence of layers 0 and 31,
+    the whole layer's codes after the quantizing append bit for bit."""
     spec = SPECS["llama8b_32l_b32_fp8"]
     case = LargeCase(spec, make_placement(spec))
-    seqs = sample_sequences(case.pl, 6, seed=21)
-    case.check_layer(0, seqs)
-    case.check_layer(spec.num_layers - 1, seqs, fused=True, early_reads=True)
+    case.check_layer(0)
+    case.check_layer(spec.num_layers - 1, fused=True, early_reads=True)
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_fp8_serving_b256_every_sequence():
+    """The E4M3 serving step at full size (a 66 GB pool): every sequence of
+    layers 0 and 31, the whole layer's codes after the append bit for bit."""
+    spec = SPECS["serving_b256_fp8"]
+    case = LargeCase(spec, make_placement(spec))
+    case.check_layer(0, fused=True, early_reads=True)
+    case.check_layer(spec.num_layers - 1)
     del case
     torch.cuda.empty_cache()
 

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import paged_kv_cache_slots_gb300 as pkv
-from gpu_harness import bits, check_output, compact_blocks, take
+from gpu_harness import bits, check_cast, check_output, compact_blocks, take
 from workloads import (SPECS, fill_pool_layer, make_placement, new_token_counts, pool_layer_values, small_spec,
                        step_token_values)
 
@@ -58,6 +58,13 @@ def _step(spec, nq, out_dtype=torch.float32, check_pool=True, scale=None):
     assert np.array_equal(slots.cpu().numpy(), o_slots), "varlen slot mapping"
     if check_pool:
         assert torch.equal(bits(kc.cpu()), bits(k_post)) and torch.equal(bits(vc.cpu()), bits(v_post))
+    if out_dtype != torch.float32:
+        # The same attention with fp32 output: the q-dtype output is it rounded to nearest even.
+        out32 = torch.full_like(out, float("nan"), dtype=torch.float32)
+        pkv.paged_prefill_attention(q.cuda(), kc, vc, tables, qs_d, ctx_d, scale, out=out32,
+                                    out_dtype=torch.float32)
+        check_output(out32, ref, f"{spec.name} prefill fp32")
+        check_cast(out, out32, f"{spec.name} prefill")
     return check_output(out, ref, f"{spec.name} prefill {out_dtype}")
 
 
@@ -107,10 +114,12 @@ def test_tensor_core_block_sizes_and_groups(block_size, group, dtype):
     _step(spec, new_token_counts(ctx, seed=group, max_chunk=200))
 
 
-def test_output_in_input_dtype():
-    spec = small_spec("prefill_out_bf16", num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
-                      dtype="bf16", seed=7, ctx=(300, 17, 1, 64))
-    _step(spec, [70, 17, 1, 5], out_dtype=torch.bfloat16)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_output_in_input_dtype(dtype, head_dim):
+    spec = small_spec(f"prefill_out_{dtype}_{head_dim}", num_q_heads=32, num_kv_heads=8, head_dim=head_dim,
+                      block_size=16, dtype=dtype, seed=7, ctx=(300, 17, 1, 64))
+    _step(spec, [70, 17, 1, 5], out_dtype=spec.torch_dtype)
 
 
 def test_long_chunk_after_context():

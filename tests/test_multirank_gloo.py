@@ -31,7 +31,10 @@ def _worker(rank, world, port, q):
     t = bench.max_over_ranks(1.5 + rank, w, "cpu")          # rank 1 is the slowest
     b = bench.sum_over_ranks(1000.0 * (rank + 1), w, "cpu")  # bytes add up over replicas
     bench.barrier(w)
-    q.put((rank, t, b))
+    # Timed regions: rank 1's regions take longer; both ranks must stop after
+    # the same region, each region counted at the slowest rank's time.
+    regions = bench.timed_regions(lambda: 40.0 + 20.0 * rank, 200.0, w, "cpu")
+    q.put((rank, t, b, tuple(regions)))
     dist.destroy_process_group()
 
 
@@ -46,10 +49,13 @@ def test_two_gloo_ranks_reduce_time_and_bytes():
         p.join(timeout=120)
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(world))
-    assert got == [(0, 2.5, 3000.0), (1, 2.5, 3000.0)]
+    assert got == [(0, 2.5, 3000.0, (60.0,) * 4), (1, 2.5, 3000.0, (60.0,) * 4)]
 
 
 def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.0, 1, "cpu") == 3.0
     assert bench.sum_over_ranks(7.0, 1, "cpu") == 7.0
+    # Regions are repeated until their sum reaches the floor (at least one).
+    assert bench.timed_regions(lambda: 30.0, 100.0, 1, "cpu") == [30.0] * 4
+    assert bench.timed_regions(lambda: 500.0, 100.0, 1, "cpu") == [500.0]
