@@ -280,14 +280,21 @@ __device__ __forceinline__ void merge_parts(const DecodeArgs& a, int s, int h, i
     }
     int c = ca;
     while (c <= cb) {
-        // This lane's part: the kp-th CTA with a non-empty item range from c on.
-        int my_c = c;
-        while (my_c <= cb && cta_is_empty(my_c, W, P)) ++my_c;
-        for (int j = 0; j < kp && my_c <= cb; ++j) {
-            ++my_c;
-            while (my_c <= cb && cta_is_empty(my_c, W, P)) ++my_c;
+        // This lane's part: the kp-th CTA with a non-empty item range from c
+        // on.  With W >= P every CTA holds items.  With fewer items than CTAs
+        // a CTA holds at most one, and the first CTA from c on that holds any
+        // holds item floor(c W / P): the kp-th is the CTA of that item + kp.
+        int my_c;
+        if (W >= P) {
+            my_c = c + kp <= cb ? c + kp : -1;
+        } else {
+            const int64_t x = static_cast<int64_t>(c) * W / P + kp;
+            my_c = -1;
+            if (x < W) {
+                const int cx = cta_of_item(x, W, P);
+                if (cx <= cb) my_c = cx;
+            }
         }
-        if (my_c > cb) my_c = -1;
         const int n = __popc(__ballot_sync(0xffffffffu, my_c >= 0 && kg == 0));
         if (n == 0) break;
         c = __shfl_sync(0xffffffffu, my_c, (n - 1) * G) + 1;
@@ -807,11 +814,8 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
         if (partial && a.fused_reduce) {
             const int ca = cta_of_item(pair_a, W, P);
             const int cb = cta_of_item(pair_b - 1, W, P);
-            int nparts = cb - ca + 1;
-            if (W < P) {
-                nparts = 0;
-                for (int c = ca; c <= cb; ++c) nparts += !cta_is_empty(c, W, P);
-            }
+            // With fewer items than CTAs each of the pair's items has its own CTA.
+            const int nparts = W >= P ? cb - ca + 1 : pair_b - pair_a;
             constexpr int T = Policy::kMaxThreads, DD = Policy::kD;
             switch (G) {
                 case 1:
