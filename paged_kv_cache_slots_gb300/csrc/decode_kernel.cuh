@@ -11,9 +11,14 @@
 // head chunk is Hc consecutive KV heads: their K rows of one block are
 // contiguous in the pool ([block][head][token][dim]), so an item is one
 // pipeline stage filled by two contiguous copies (K, V) of Hc*bs*D elements.
-// Items are ordered sequence-major; W = chunks * sum_s ceil(ctx_s / bs).
-// CTA c of P owns items [c*W/P, (c+1)*W/P): every CTA streams the same number
-// of items (to within one) whatever the length mix.  The run of one (sequence,
+// Items are ordered sequence-major, and every (sequence, head chunk) pair
+// starts with `phantom` items without data (a stage the producer completes
+// without a copy, skipped by the consumers), so that a CTA whose range
+// crosses into a pair -- and pays for the switch: a partial's stores, the
+// merge arrival's fence, the next q -- takes that many fewer blocks.
+// W = chunks * sum_s (ceil(ctx_s / bs) + phantom) over the sequences with
+// tokens.  CTA c of P owns items [c*W/P, (c+1)*W/P): every CTA streams the
+// same number of items (to within one) whatever the length mix.  The run of one (sequence,
 // head chunk) pair inside one CTA is a segment.  A segment covering its whole
 // pair writes the final output; otherwise it writes fp32 partials
 // (unnormalised O, running max, running sum) to slot c + pair, unique because
@@ -103,7 +108,8 @@ __device__ __forceinline__ int clamp_context(const DecodeArgs& a, int s, bool fl
     return c;
 }
 
-// cum[s] = chunks * sum_{s' < s} ceil(ctx_s' / bs); cum[num_seqs] = W.
+// cum[s] = chunks * sum_{s' < s, ctx_s' > 0} (ceil(ctx_s' / bs) + phantom);
+// cum[num_seqs] = W.
 static __device__ void build_prefix(const DecodeArgs& a, int chunks, int32_t* cum, int32_t* scan) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -113,7 +119,8 @@ static __device__ void build_prefix(const DecodeArgs& a, int chunks, int32_t* cu
         int v = 0;
         if (s < a.num_seqs) {
             const int c = clamp_context(a, s, blockIdx.x == 0);
-            v = (c + a.block_size - 1) / a.block_size * chunks;
+            const int nb = (c + a.block_size - 1) / a.block_size;
+            v = nb > 0 ? (nb + a.phantom) * chunks : 0;
         }
         int x = v;
 #pragma unroll
@@ -159,19 +166,21 @@ static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* ful
     bool ok = true;
     for (int base = start; base < end && ok; base += 32) {
         const int i = base + lane;
-        int64_t row = 0;  // first pool row of the item: (blk * Hkv + hc * Hc) * bs
+        int64_t row = -1;  // first pool row of the item: (blk * Hkv + hc * Hc) * bs; -1: no data
         if (i < end) {
             const int s = find_sequence(cum, a.num_seqs, i);
-            const int nb = (cum[s + 1] - cum[s]) / chunks;
+            const int nbv = (cum[s + 1] - cum[s]) / chunks;  // the pair's items, phantoms included
             const int r = i - cum[s];
-            const int hc = r / nb;
-            const int j = r - hc * nb;
-            int blk = __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks + j);
-            if (blk < 0 || blk >= a.num_blocks) {
-                raise_flag(a.status, kFlagBadBlock);
-                blk = 0;
+            const int hc = r / nbv;
+            const int j = r - hc * nbv - a.phantom;
+            if (j >= 0) {
+                int blk = __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks + j);
+                if (blk < 0 || blk >= a.num_blocks) {
+                    raise_flag(a.status, kFlagBadBlock);
+                    blk = 0;
+                }
+                row = (static_cast<int64_t>(blk) * a.num_kv_heads + hc * a.heads_per_stage) * a.block_size;
             }
-            row = (static_cast<int64_t>(blk) * a.num_kv_heads + hc * a.heads_per_stage) * a.block_size;
         }
         // With early reads the cache is not written by the launch still
         // running, and this CTA typically starts while that launch's last
@@ -182,7 +191,7 @@ static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* ful
         // saved (batch-32 step -2.6 %); with hundreds (a layer of ~550 us)
         // the step gained 1.6 %.
         if (a.early_reads && base == start && end - start >= kPrefetchMinItems && lane >= a.stages &&
-            lane < a.stages + kPrefetchItems && i < end) {
+            lane < a.stages + kPrefetchItems && i < end && row >= 0) {
             const int64_t off = row * row_bytes;
             prefetch_l2(static_cast<const char*>(a.k_cache) + off, half_bytes);
             prefetch_l2(static_cast<const char*>(a.v_cache) + off, half_bytes);
@@ -197,7 +206,10 @@ static __device__ void produce(const DecodeArgs& a, uint8_t* ring, uint64_t* ful
                 if (a.test_stall && blockIdx.x == 0 && base + k - start == 1) good = 0;
                 if (good && round > 0)
                     good = mbar_wait_bounded(&empty[stage], (round - 1) & 1, abort, a.status);
-                if (good) {
+                if (good && rk < 0) {  // a phantom item: the stage completes without data
+                    mbar_arrive(&full[stage]);
+                    ++issued;
+                } else if (good) {
                     uint8_t* kd = ring + stage * stage_bytes;
                     uint8_t* vd = kd + half_bytes;
                     mbar_arrive_expect_tx(&full[stage], stage_bytes);
@@ -712,10 +724,11 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
     int seg = start;
     while (seg < end) {
         const int s = find_sequence(cum, a.num_seqs, seg);
-        const int nb = (cum[s + 1] - cum[s]) / chunks;
-        const int hc = (seg - cum[s]) / nb;
-        const int pair_a = cum[s] + hc * nb;
-        const int pair_b = pair_a + nb;
+        const int nbv = (cum[s + 1] - cum[s]) / chunks;  // the pair's items, phantoms included
+        const int nb = nbv - a.phantom;                    // its blocks
+        const int hc = (seg - cum[s]) / nbv;
+        const int pair_a = cum[s] + hc * nbv;
+        const int pair_b = pair_a + nbv;
         const int seg_end = min(pair_b, end);
         const int h = hc * Hc + hw;
         const int ctx = clamp_context(a, s, false);
@@ -731,9 +744,10 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
             // Waiting for the second while holding the first needs the
             // producer to have refilled stage (i + R) % stages, i.e. item
             // i + R - stages to be released: true when stages >= 2R.
+            const int j = i - pair_a - a.phantom;  // block index; negative: a phantom item
             bool two = false;
             if constexpr (Policy::kPairs)
-                two = a.block_size == 16 && i + R < seg_end && a.stages >= 2 * R;
+                two = a.block_size == 16 && i + R < seg_end && a.stages >= 2 * R && j >= 0;
             int stage2 = stage + R;  // R divides the ring size, so this wraps exactly at the end
             uint32_t phase2 = phase;
             if (stage2 >= a.stages) {
@@ -742,8 +756,7 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
             }
             bool ok = mbar_wait_bounded(&full[stage], phase, abort, a.status);
             if (ok && two) ok = mbar_wait_bounded(&full[stage2], phase2, abort, a.status);
-            if (ok) {
-                const int j = i - pair_a;
+            if (ok && j >= 0) {
                 const int n_valid = min(a.block_size, ctx - j * a.block_size);
                 uint8_t* kt = ring + stage * 2 * half_bytes;
                 bool patched = a.k_new && j == nb - 1 && append_row(a, pol, kt, kt + half_bytes, s, h, hw, j, n_valid - 1);
@@ -776,11 +789,17 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
                 }
             }
         }
-        const bool whole = (pair_a >= start) && (pair_b <= end);
+        // The pair's blocks are its items [pair_r, pair_b) (phantoms first).
+        // A segment holding none of them is not a part of the pair: it
+        // writes nothing and counts no arrival (the same on every warp).
+        const int pair_r = pair_a + a.phantom;
+        const bool whole = (pair_r >= start) && (pair_b <= end);
+        const bool blocks = max(seg, pair_r) < seg_end;
         const int pair = s * chunks + hc;
         const int64_t sl = (static_cast<int64_t>(blockIdx.x + pair) * Hc + hw) * G;
         bool partial = false;  // this warp wrote the CTA's partial of (s, h)
-        if (R == 1) {
+        if (!blocks) {
+        } else if (R == 1) {
             if (!*abort) {
                 if (whole) {
                     pol.write_final(st, a, s, h, G);
@@ -806,16 +825,17 @@ __global__ void __launch_bounds__(Policy::kMaxThreads, 1)
         // the parts there, one slice a warp.
         float* staging = nullptr;
         int staging_floats = 0;
-        if (R == 1 && a.fused_reduce && seg_end == end && !whole) {
+        if (R == 1 && a.fused_reduce && seg_end == end && !whole && blocks) {
             named_barrier_sync(1, NC * 32);
             staging_floats = (a.stages * 2 * half_bytes / NC / 4) & ~3;
             staging = reinterpret_cast<float*>(ring) + w * staging_floats;
         }
         if (partial && a.fused_reduce) {
-            const int ca = cta_of_item(pair_a, W, P);
+            // The parts: the CTAs holding the pair's blocks.  With fewer
+            // items than CTAs each block has its own CTA.
+            const int ca = cta_of_item(pair_r, W, P);
             const int cb = cta_of_item(pair_b - 1, W, P);
-            // With fewer items than CTAs each of the pair's items has its own CTA.
-            const int nparts = W >= P ? cb - ca + 1 : pair_b - pair_a;
+            const int nparts = W >= P ? cb - ca + 1 : pair_b - pair_r;
             constexpr int T = Policy::kMaxThreads, DD = Policy::kD;
             switch (G) {
                 case 1:

@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeAr
     const int D = a.head_dim, Hc = a.heads_per_stage;
     const int chunks = a.num_kv_heads / Hc;
     const int hc = h / Hc, hw = h - hc * Hc;
-    const int nb = (a.cum[s + 1] - a.cum[s]) / chunks;
+    const int nbv = (a.cum[s + 1] - a.cum[s]) / chunks;  // the pair's items, phantoms first
+    const int nb = nbv > 0 ? nbv - a.phantom : 0;       // its blocks
     const int64_t out0 = (static_cast<int64_t>(s) * a.num_q_heads + h * G) * D;
     const int tid = threadIdx.x;
     if (nb == 0) {
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeAr
     }
     const int64_t W = a.cum[a.num_seqs];
     const int64_t P = a.num_ctas;
-    const int64_t pa = a.cum[s] + static_cast<int64_t>(hc) * nb;
+    const int64_t pa = a.cum[s] + static_cast<int64_t>(hc) * nbv + a.phantom;  // its first block
     const int ca = cta_of_item(pa, W, a.num_ctas);
     const int cb = cta_of_item(pa + nb - 1, W, a.num_ctas);
     if (ca == cb) return;

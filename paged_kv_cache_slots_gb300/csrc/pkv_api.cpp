@@ -631,6 +631,19 @@ static kv_status_t decode_impl(const void* q, const void* k_cache, const void* v
     a.pdl = o.no_pdl ? 0 : 1;
     a.early_reads = (o.early_reads && !o.no_pdl) ? 1 : 0;
     a.test_stall = o.test_stall;
+    // Phantom items per pair: about the time a CTA loses switching to the
+    // next pair (the partial's stores, the merge arrival's release fence,
+    // the next q: 3-5 us measured) in stages' worth of streaming, i.e.
+    // 300 KiB of stage data: 5 items for 64 KiB stages, 8 (the cap) for the
+    // E4M3 stages of 32 KiB (the best of 0, 100, 200, 300 and 400 KiB in an
+    // A/B on one box).  Not with too few items to split (fewer than two a
+    // CTA even with every table entry used).
+    {
+        const int64_t stage_bytes = 2 * static_cast<int64_t>(plan.stage_half_bytes);
+        const int64_t max_items = static_cast<int64_t>(num_seqs) * (num_kv_heads / hc) * max_blocks;
+        int ph = static_cast<int>((int64_t{300} * 1024 + stage_bytes / 2) / stage_bytes);
+        a.phantom = max_items >= 2 * static_cast<int64_t>(P) ? (ph > 8 ? 8 : ph) : 0;
+    }
     a.device = dev;
     a.k_new = k_new;
     a.v_new = v_new;

@@ -60,8 +60,13 @@ struct SlotArgs {
 // Work items are (sequence, head chunk, logical block) triples in that order;
 // a head chunk is `heads_per_stage` consecutive KV heads, whose K (and V)
 // rows of one block are contiguous in the pool, so one item is one pipeline
-// stage of two contiguous copies.  W = chunks * sum_s ceil(ctx_s / bs);
-// CTA c of num_ctas owns items [c*W/P, (c+1)*W/P).
+// stage of two contiguous copies.  Every pair (sequence, head chunk) with
+// blocks starts with `phantom` items that carry no data (a ring stage that
+// the producer completes without a copy and the consumers skip): a CTA whose
+// range crosses into a pair takes that many fewer blocks, which pays for the
+// switch between pairs.  W = chunks * sum_s (ceil(ctx_s / bs) + phantom,
+// over the sequences with tokens); CTA c of num_ctas owns items
+// [c*W/P, (c+1)*W/P).
 struct DecodeArgs {
     const void* q;
     const void* k_cache;
@@ -96,6 +101,7 @@ struct DecodeArgs {
     int early_reads;      // 1: tables, lengths and cache may be read before the previous launch ends
     int test_stall;       // testing only: see kv_decode_options_t
     int device;           // CUDA ordinal the launch targets
+    int phantom;          // items without data at the start of every (sequence, head chunk) pair
 };
 
 // Multi-token (chunked-prefill) attention and its plan.
