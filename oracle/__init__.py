@@ -86,6 +86,9 @@ def load(path: str | None = None):
         lib.oracle_paged_prefill.argtypes = [c_i, c_p, c_p, c_p, c_p, c_i, c_p, c_p, c_i, c_i, c_i, c_i,
                                              c_i, c_i, c_d, c_p, c_i]
         lib.oracle_paged_prefill.restype = c_i
+        lib.oracle_paged_prefill_scaled.argtypes = [c_i, c_i, c_d, c_d, c_p, c_p, c_p, c_p, c_i, c_p, c_p, c_i,
+                                                    c_i, c_i, c_i, c_i, c_i, c_d, c_p, c_i]
+        lib.oracle_paged_prefill_scaled.restype = c_i
         lib.oracle_slot_mapping_varlen.argtypes = [c_p, c_i, c_p, c_p, c_i, c_i, c_p]
         lib.oracle_slot_mapping_varlen.restype = None
         lib.oracle_num_cores.argtypes = []
@@ -243,12 +246,16 @@ def slot_mapping_varlen(block_tables, query_start, context_lens, block_size: int
 
 
 def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, scale: float,
-                  nthreads: int = 0, lib=None) -> np.ndarray:
-    """fp64 output [T, Hq, D] of multi-token (causal) queries over the paged cache."""
+                  nthreads: int = 0, lib=None, k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
+    """fp64 output [T, Hq, D] of multi-token (causal) queries over the paged cache.
+
+    An E4M3 cache stands for k_scale (v_scale) times its codes' values; other
+    caches share q's dtype and take no scales."""
     lib = lib or load()
     dt = _dtype_name(k_cache)
-    if _dtype_name(q) != dt:
-        raise ValueError("q and the cache must share a dtype")
+    qdt = _dtype_name(q)
+    if dt != "e4m3" and (qdt != dt or k_scale != 1.0 or v_scale != 1.0):
+        raise ValueError("q and a non-E4M3 cache must share a dtype and take no scales")
     qa, kc, vc = _raw(q), _raw(k_cache), _raw(v_cache)
     t = np.ascontiguousarray(block_tables, dtype=np.int32)
     qs = np.ascontiguousarray(query_start, dtype=np.int32)
@@ -258,11 +265,11 @@ def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, 
     B = len(c)
     assert D == D2 and t.shape[0] == B and len(qs) == B + 1 and int(qs[-1]) == T
     out = np.empty((T, Hq, D), dtype=np.float64)
-    rc = lib.oracle_paged_prefill(DTYPE_CODE[dt], _ptr(qa), _ptr(kc), _ptr(vc), _ptr(t), t.shape[1],
-                                  _ptr(qs), _ptr(c), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(out),
-                                  nthreads)
+    rc = lib.oracle_paged_prefill_scaled(DTYPE_CODE[qdt], DTYPE_CODE[dt], float(k_scale), float(v_scale),
+                                         _ptr(qa), _ptr(kc), _ptr(vc), _ptr(t), t.shape[1], _ptr(qs), _ptr(c), B,
+                                         Hq, Hkv, D, bs, NB, float(scale), _ptr(out), nthreads)
     if rc != 0:
-        raise ValueError(f"oracle_paged_prefill failed ({rc})")
+        raise ValueError(f"oracle_paged_prefill_scaled failed ({rc})")
     return out
 
 

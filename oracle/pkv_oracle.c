@@ -316,7 +316,8 @@ int oracle_paged_decode_scaled(int q_dtype, int kv_dtype, double k_scale, double
  * positions 0 .. context_lens[s] - n_s + i: softmax(scale q.K^T).V over that
  * causal prefix, read through the block table, fp64. */
 typedef struct {
-    int dtype;
+    int q_dtype, kv_dtype;
+    double k_scale, v_scale; /* a cache element stands for scale * its stored value */
     const void *q, *k_cache, *v_cache;
     const int32_t *tables, *qstart, *ctx;
     int max_blocks, num_seqs, hq, hkv, d, bs, num_blocks;
@@ -346,14 +347,14 @@ static void* orc_prefill_rows(void* arg) {
             cap = last + 1;
             x = (double*)realloc(x, sizeof(double) * (size_t)cap);
         }
-        for (int d = 0; d < D; ++d) qd[d] = orc_load(J->q, (size_t)r * D + d, J->dtype);
+        for (int d = 0; d < D; ++d) qd[d] = orc_load(J->q, (size_t)r * D + d, J->q_dtype);
         double mx = -INFINITY;
         for (int t = 0; t <= last; ++t) { /* scores over the causal prefix */
             int64_t blk = J->tables[(int64_t)s * J->max_blocks + t / J->bs];
             if (blk < 0 || blk >= J->num_blocks) { J->status = -1; blk = 0; }
             size_t base = (size_t)(((blk * J->hkv + h) * J->bs + t % J->bs)) * D;
             double acc = 0.0;
-            for (int d = 0; d < D; ++d) acc += qd[d] * orc_load(J->k_cache, base + d, J->dtype);
+            for (int d = 0; d < D; ++d) acc += qd[d] * (J->k_scale * orc_load(J->k_cache, base + d, J->kv_dtype));
             x[t] = J->scale * acc;
             if (x[t] > mx) mx = x[t];
         }
@@ -367,7 +368,7 @@ static void* orc_prefill_rows(void* arg) {
             if (blk < 0 || blk >= J->num_blocks) blk = 0;
             size_t base = (size_t)(((blk * J->hkv + h) * J->bs + t % J->bs)) * D;
             double w = x[t] / sum;
-            for (int d = 0; d < D; ++d) o[d] += w * orc_load(J->v_cache, base + d, J->dtype);
+            for (int d = 0; d < D; ++d) o[d] += w * (J->v_scale * orc_load(J->v_cache, base + d, J->kv_dtype));
         }
     }
     free(x);
@@ -375,14 +376,16 @@ static void* orc_prefill_rows(void* arg) {
     return NULL;
 }
 
-/* out[T][Hq][D] (fp64) of the multi-token queries described above.  Returns
- * 0, -1 for a table entry outside the pool or a chunk longer than its context,
- * -2 for bad head counts. */
-int oracle_paged_prefill(int dtype, const void* q, const void* k_cache, const void* v_cache,
-                         const int32_t* block_tables, int max_blocks, const int32_t* query_start,
-                         const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
-                         int head_dim, int block_size, int num_blocks, double scale, double* out,
-                         int nthreads) {
+/* out[T][Hq][D] (fp64) of the multi-token queries described above, q in
+ * q_dtype, the cache in kv_dtype, a cache element standing for k_scale
+ * (v_scale) times its stored value (an E4M3 cache with its per-layer scales,
+ * as in oracle_paged_decode_scaled).  Returns 0, -1 for a table entry outside
+ * the pool or a chunk longer than its context, -2 for bad head counts. */
+int oracle_paged_prefill_scaled(int q_dtype, int kv_dtype, double k_scale, double v_scale, const void* q,
+                                const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                                int max_blocks, const int32_t* query_start, const int32_t* context_lens,
+                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, double scale, double* out, int nthreads) {
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return -2;
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;
@@ -391,9 +394,9 @@ int oracle_paged_prefill(int dtype, const void* q, const void* k_cache, const vo
     orc_pjob* jobs = (orc_pjob*)calloc((size_t)nthreads, sizeof(orc_pjob));
     pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int i = 0; i < nthreads; ++i) {
-        orc_pjob j = {dtype, q, k_cache, v_cache, block_tables, query_start, context_lens, max_blocks,
-                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
-                      rows * i / nthreads, rows * (i + 1) / nthreads, 0};
+        orc_pjob j = {q_dtype, kv_dtype, k_scale, v_scale, q, k_cache, v_cache, block_tables, query_start,
+                      context_lens, max_blocks, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, scale, out, rows * i / nthreads, rows * (i + 1) / nthreads, 0};
         jobs[i] = j;
     }
     for (int i = 1; i < nthreads; ++i) pthread_create(&th[i], NULL, orc_prefill_rows, &jobs[i]);
@@ -406,6 +409,17 @@ int oracle_paged_prefill(int dtype, const void* q, const void* k_cache, const vo
     free(jobs);
     free(th);
     return status;
+}
+
+/* The same with q and the cache in one dtype and no cache scaling. */
+int oracle_paged_prefill(int dtype, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, double scale, double* out,
+                         int nthreads) {
+    return oracle_paged_prefill_scaled(dtype, dtype, 1.0, 1.0, q, k_cache, v_cache, block_tables, max_blocks,
+                                       query_start, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                       block_size, num_blocks, scale, out, nthreads);
 }
 
 /* Slot of every new token: token i of sequence s sits at position

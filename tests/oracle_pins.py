@@ -457,6 +457,39 @@ def check_prefill_chunking_and_decode(lib):
     assert np.array_equal(dec, whole[20:21]), "one new token = decode"
 
 
+def check_fp8_prefill(lib):
+    # Multi-token queries over an E4M3 cache with power-of-two scales: every
+    # dequantized value (scale times the code's value) is exact in f32, so the
+    # same step over an f32 cache holding those values must agree to rounding;
+    # and one new token per sequence is the E4M3 decode step, bit for bit.
+    rng = np.random.default_rng(65)
+    ctx, nq = [9, 1, 30, 17], [4, 1, 11, 17]
+    Hq, Hkv, D, bs = 8, 2, 16, 4
+    NB = sum((c + bs - 1) // bs for c in ctx) + 3
+    tables = _random_tables(rng, ctx, bs, NB)
+    kp = torch.from_numpy(rng.integers(0, 256, (NB, Hkv, bs, D), dtype=np.uint8))
+    vp = torch.from_numpy(rng.integers(0, 256, (NB, Hkv, bs, D), dtype=np.uint8))
+    kp[(kp & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    vp[(vp & 0x7F) == 0x7F] = 0x44
+    k8, v8 = kp.view(torch.float8_e4m3fn), vp.view(torch.float8_e4m3fn)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    T = int(qs[-1])
+    q = torch.from_numpy(rng.standard_normal((T, Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    ks, vs, scale = 2.0 ** -6, 2.0 ** -3, 0.3
+    c = np.array(ctx, np.int32)
+    got = oracle.paged_prefill(q, k8, v8, tables, qs, c, scale, lib=lib, k_scale=ks, v_scale=vs)
+    kf = (ks * k8.to(torch.float64)).to(torch.float32)
+    vf = (vs * v8.to(torch.float64)).to(torch.float32)
+    ref = oracle.paged_prefill(q.float(), kf, vf, tables, qs, c, scale, lib=lib)
+    assert np.max(np.abs(got - ref)) < 1e-12, "E4M3 prefill vs the f32 prefill over the dequantized cache"
+    one = np.arange(len(ctx) + 1, dtype=np.int32)
+    qd = q[qs[1:] - 1]  # each sequence's last new token
+    dec = oracle.paged_decode(qd, k8, v8, tables, c, scale, lib=lib, k_scale=ks, v_scale=vs)
+    pre = oracle.paged_prefill(qd, k8, v8, tables, one, c, scale, lib=lib, k_scale=ks, v_scale=vs)
+    assert np.array_equal(pre, dec), "one new token over an E4M3 cache = the E4M3 decode step"
+    assert np.array_equal(pre, got[qs[1:] - 1]), "the last token of each chunk"
+
+
 def check_varlen_slots(lib):
     # The worked slots of "vLLM Architecture and Installation", Example 3:
     # A (table [1, 2, 3, 6]) positions 9..12 -> 13, 14, 15, 24; B ([4, 5]) position 7 -> 23.
@@ -472,4 +505,4 @@ ALL_CHECKS = [check_f16_decoder, check_bf16_decoder, check_f32_decoder, check_wo
               check_append_roundtrip, check_bruteforce, check_closed_forms,
               check_relabel_and_heads, check_e4m3_decoder, check_e4m3_encoder, check_fp8_append,
               check_fp8_attention, check_prefill_vs_torch_sdpa, check_prefill_bruteforce_with_context,
-              check_prefill_chunking_and_decode, check_varlen_slots]
+              check_prefill_chunking_and_decode, check_fp8_prefill, check_varlen_slots]

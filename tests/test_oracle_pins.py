@@ -30,8 +30,8 @@ MUTATIONS = [
     ("last_token_dropped", "for (int t = 0; t < n; ++t) {\n            double w",
      "for (int t = 0; t + 1 < n; ++t) {\n            double w"),
     ("keys_as_values", "o[d] += w * V[", "o[d] += w * K["),
-    ("q_row_of_kv_head", "qd[d] = orc_load(J->q, (size_t)r * D + d, J->q_dtype);",
-     "qd[d] = orc_load(J->q, ((size_t)s * J->hq + h) * D + d, J->q_dtype);"),
+    ("q_row_of_kv_head", "qd[d] = orc_load(J->q, (size_t)r * D + d, J->q_dtype);\n        /* 2. scores */",
+     "qd[d] = orc_load(J->q, ((size_t)s * J->hq + h) * D + d, J->q_dtype);\n        /* 2. scores */"),
     ("append_transposed_layout",
      "size_t dst = (size_t)(((blk * num_kv_heads + h) * block_size + off)) * row;",
      "size_t dst = (size_t)(((blk * block_size + off) * num_kv_heads + h)) * row;"),
@@ -52,6 +52,11 @@ MUTATIONS = [
     ("prefill_no_causal_mask", "int last = J->ctx[s] - n + i; /* position", "int last = J->ctx[s] - 1; /* position"),
     ("prefill_head_modulo", "int g = (int)(r % J->hq), h = g / G;", "int g = (int)(r % J->hq), h = g % J->hkv;"),
     ("varlen_slot_offset", "context_lens[s] - n + i, block_size);", "context_lens[s] - n + i + 1, block_size);"),
+    ("prefill_k_with_v_scale", "acc += qd[d] * (J->k_scale * orc_load(J->k_cache",
+     "acc += qd[d] * (J->v_scale * orc_load(J->k_cache"),
+    ("prefill_v_unscaled", "o[d] += w * (J->v_scale * orc_load(J->v_cache", "o[d] += w * (1.0 * orc_load(J->v_cache"),
+    ("prefill_q_read_as_cache_type", "qd[d] = orc_load(J->q, (size_t)r * D + d, J->q_dtype);\n        double mx",
+     "qd[d] = orc_load(J->q, (size_t)r * D + d, J->kv_dtype);\n        double mx"),
 ]
 
 
