@@ -333,13 +333,16 @@ size_t paged_prefill_workspace_bytes(int num_seqs);
  * append): row t = query_start[s] + i of q and out ([num_tokens][Hq][D])
  * attends to the cached tokens of s at positions 0 .. context_lens[s] - n_s + i,
  * softmax(scale q.K^T).V with fp32 accumulation; query head g reads KV head
- * g / (Hq/Hkv).  dtype f16 or bf16 (q and the cache), head_dim 64 or 128,
- * block_size a multiple of 16 up to 256, Hq/Hkv in {1, 2, 4, 8}; out_dtype
- * KV_F32 or dtype.  A sequence with n_s > context_lens[s] (or a length past
- * its table) is skipped (its rows are not written) and sets
- * KV_FLAG_BAD_CONTEXT.  One CTA per (16 new tokens, KV head); a decoding
- * sequence (n_s = 1) is served too, but paged_decode_attention is the faster
- * call for a batch of those. */
+ * g / (Hq/Hkv).  dtype f16 or bf16 (q and the cache; block_size a multiple
+ * of 16 up to 256) or f32 (block_size 1 .. 256; CUDA-core kernel, one warp
+ * per token and query head, not tuned for speed), head_dim 64 or 128, Hq/Hkv
+ * in {1, 2, 4, 8}; out_dtype KV_F32 or dtype.  A sequence with
+ * n_s > context_lens[s] (or a length past its table) is skipped (its rows
+ * are not written) and sets KV_FLAG_BAD_CONTEXT.  One CTA per (16 new
+ * tokens, KV head) for f16/bf16; a decoding sequence (n_s = 1) is served
+ * too, but paged_decode_attention is the faster call for a batch of those.
+ * An E4M3 cache goes to paged_prefill_attention_fp8 (KV_ERR_INVALID_ARG
+ * here). */
 kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
                                     int num_blocks, const int32_t* block_tables,
                                     int max_blocks_per_seq, const int32_t* query_start,
@@ -350,6 +353,22 @@ kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const vo
                                     void* stream);
 
 /* ------------------------------------------------------- FP8 (E4M3) cache */
+
+/* paged_prefill_attention over a KV_FP8_E4M3 cache ("vLLM Architecture and
+ * Installation", Example 6, with the chunked prefill of Example 5): the keys
+ * and values are k_scale (v_scale) times their codes' values.  q_dtype
+ * KV_F16 or KV_BF16, head_dim 128, block_size a multiple of 16 up to 256;
+ * out_dtype KV_F32 or q_dtype; the rest as paged_prefill_attention.  Each
+ * block's codes are converted exactly to q's type in shared memory and the
+ * scales folded into the score multiplier and the output. */
+kv_status_t paged_prefill_attention_fp8(const void* q, kv_dtype_t q_dtype, const void* k_cache,
+                                        const void* v_cache, float k_scale, float v_scale,
+                                        int num_blocks, const int32_t* block_tables,
+                                        int max_blocks_per_seq, const int32_t* query_start,
+                                        const int32_t* context_lens, int num_seqs, int num_tokens,
+                                        int num_q_heads, int num_kv_heads, int head_dim,
+                                        int block_size, float scale, void* out, kv_dtype_t out_dtype,
+                                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* kv_append into a KV_FP8_E4M3 pool: k and v are [n_tokens][Hkv][D] rows in
  * src_dtype (KV_F32, KV_F16 or KV_BF16); each value x is stored as the E4M3

@@ -107,6 +107,8 @@ def _declare(lib):
         "kv_slot_mapping_varlen": (I, [P, I, P, P, I, I, I, I, P, P]),
         "paged_prefill_attention": (I, [P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, ctypes.c_float, P, I,
                                         P, SZ, P]),
+        "paged_prefill_attention_fp8": (I, [P, I, P, P, ctypes.c_float, ctypes.c_float, I, P, I, P, P, I, I, I,
+                                            I, I, I, ctypes.c_float, P, I, P, SZ, P]),
         "kv_swap_bytes": (SZ, [P, I]),
         "kv_swap_out": (I, [P, P, I, P, SZ, P]),
         "kv_swap_in": (I, [P, P, I, P, SZ, P]),
@@ -490,15 +492,21 @@ def slot_mapping_varlen(block_tables: torch.Tensor, query_start: torch.Tensor, c
 
 
 def paged_prefill_attention(q, k_cache, v_cache, block_tables, query_start, context_lens, scale: float,
-                            out=None, out_dtype=None, workspace=None, stream=None):
+                            out=None, out_dtype=None, workspace=None, stream=None, k_scale=None, v_scale=None):
     """Causal attention of a step's new tokens (q [T, Hq, D], rows grouped by
-    sequence as query_start says) over the paged cache they were appended to."""
+    sequence as query_start says) over the paged cache they were appended to.
+    E4M3 (torch.float8_e4m3fn) caches stand for k_scale (v_scale) times their codes."""
     lib = load_library()
     T, Hq, D = q.shape
     NB, Hkv, bs, D2 = k_cache.shape
     B = context_lens.shape[0]
     _need(D == D2 and tuple(v_cache.shape) == tuple(k_cache.shape), "cache shapes")
-    _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and the caches share a dtype")
+    fp8 = k_cache.dtype == FP8
+    if fp8:
+        _need(v_cache.dtype == FP8 and k_scale is not None and v_scale is not None,
+              "an E4M3 cache needs both caches E4M3 and k_scale, v_scale")
+    else:
+        _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and the caches share a dtype")
     _need(all(t.is_contiguous() for t in (q, k_cache, v_cache, block_tables, query_start, context_lens)),
           "contiguous inputs")
     _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32 and
@@ -511,6 +519,13 @@ def paged_prefill_attention(q, k_cache, v_cache, block_tables, query_start, cont
     if workspace is None:
         workspace = torch.empty(max(16, int(lib.paged_prefill_workspace_bytes(B))), dtype=torch.uint8,
                                 device=q.device)
+    if fp8:
+        _call_on(q, lib, lib.paged_prefill_attention_fp8,
+                 _ptr(q), DTYPE_CODE[q.dtype], _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale), NB,
+                 _ptr(block_tables), block_tables.shape[1], _ptr(query_start), _ptr(context_lens), B, T, Hq, Hkv,
+                 D, bs, float(scale), _ptr(out), DTYPE_CODE[out_dtype], _ptr(workspace), workspace.numel(),
+                 _stream(q, stream))
+        return out
     _call_on(q, lib, lib.paged_prefill_attention,
         _ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), block_tables.shape[1],
         _ptr(query_start), _ptr(context_lens), B, T, Hq, Hkv, D, bs, DTYPE_CODE[q.dtype], float(scale),

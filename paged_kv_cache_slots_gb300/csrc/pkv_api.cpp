@@ -767,12 +767,13 @@ kv_status_t kv_slot_mapping_varlen(const int32_t* block_tables, int max_blocks, 
     return KV_OK;
 }
 
-kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
-                                    const int32_t* block_tables, int max_blocks, const int32_t* query_start,
-                                    const int32_t* context_lens, int num_seqs, int num_tokens, int num_q_heads,
-                                    int num_kv_heads, int head_dim, int block_size, kv_dtype_t dtype,
-                                    float scale, void* out, kv_dtype_t out_dtype, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
+static kv_status_t prefill_impl(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                                const int32_t* context_lens, int num_seqs, int num_tokens, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, kv_dtype_t dtype,
+                                kv_dtype_t kv_dtype, float k_scale, float v_scale, float scale, void* out,
+                                kv_dtype_t out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    const bool fp8 = kv_dtype == KV_FP8_E4M3;
     if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
         max_blocks <= 0)
         return fail(KV_ERR_INVALID_ARG, "paged_prefill_attention: sizes out of range");
@@ -783,10 +784,21 @@ kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const vo
     if (G != 1 && G != 2 && G != 4 && G != 8)
         return fail(KV_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", G);
     if (head_dim != 64 && head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "head_dim %d", head_dim);
-    if (block_size % 16 || block_size < 16 || block_size > 256)
-        return fail(KV_ERR_UNSUPPORTED, "multi-token queries need block_size a multiple of 16 up to 256");
-    if (dtype != KV_F16 && dtype != KV_BF16)
-        return fail(KV_ERR_UNSUPPORTED, "multi-token queries run on f16 or bf16");
+    if (dtype == KV_F32 && !fp8) {
+        if (block_size < 1 || block_size > 256)
+            return fail(KV_ERR_UNSUPPORTED, "block_size must be 1 .. 256");
+    } else if (block_size % 16 || block_size < 16 || block_size > 256) {
+        return fail(KV_ERR_UNSUPPORTED, "multi-token queries on f16/bf16 need block_size a multiple of 16 up to 256");
+    }
+    if (fp8) {
+        if (dtype != KV_F16 && dtype != KV_BF16)
+            return fail(KV_ERR_UNSUPPORTED, "an E4M3 cache takes an f16 or bf16 q");
+        if (head_dim != 128) return fail(KV_ERR_UNSUPPORTED, "an E4M3 cache needs head_dim 128");
+        if (!valid_scale(k_scale) || !valid_scale(v_scale))
+            return fail(KV_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
+    } else if (dtype != KV_F32 && dtype != KV_F16 && dtype != KV_BF16) {
+        return fail(KV_ERR_INVALID_ARG, "unknown dtype");
+    }
     if (out_dtype != KV_F32 && out_dtype != dtype)
         return fail(KV_ERR_UNSUPPORTED, "out_dtype must be KV_F32 or the input dtype");
     if (!std::isfinite(scale)) return fail(KV_ERR_INVALID_ARG, "scale is not finite");
@@ -804,13 +816,16 @@ kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const vo
     int dev = 0, max_smem = 0;
     uint32_t* status = nullptr;
     if (kv_status_t st = device_info(&dev, &status, nullptr, &max_smem, nullptr)) return st;
-    // The tcgen05 kernel: head_dim 128 and blocks that tile 64-key tiles evenly.
-    const bool tc = head_dim == 128 && (block_size % 64 == 0 || 64 % block_size == 0) &&
-                    prefill_tc_smem_bytes() <= max_smem;
+    // The tcgen05 kernel: f16/bf16 cache, head_dim 128, blocks that tile 64-key tiles evenly.
+    const bool tc = !fp8 && dtype != KV_F32 && head_dim == 128 &&
+                    (block_size % 64 == 0 || 64 % block_size == 0) && prefill_tc_smem_bytes() <= max_smem;
+    // Stages of the warp-MMA kernel hold K and V in q's 2-byte type (an E4M3
+    // block converted); E4M3 adds two raw slots of codes.
     const int stage_bytes = 2 * block_size * head_dim * 2;
-    int stages = (max_smem - 1024 - 64) / stage_bytes;
+    const int raw_bytes = fp8 ? 4 * block_size * head_dim : 0;
+    int stages = (max_smem - 2048 - 64 - raw_bytes) / stage_bytes;
     if (stages > 4) stages = 4;
-    if (!tc && stages < 2) return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages");
+    if (!tc && dtype != KV_F32 && stages < 2) return fail(KV_ERR_UNSUPPORTED, "shared memory cannot hold two stages");
     PrefillArgs a{};
     a.q = q;
     a.k_cache = k_cache;
@@ -831,9 +846,14 @@ kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const vo
     a.block_size = block_size;
     a.dtype = dtype;
     a.out_dtype = out_dtype;
-    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.kv_dtype = fp8 ? KV_FP8_E4M3 : dtype;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 *
+                                      static_cast<double>(fp8 ? k_scale : 1.f));
+    a.v_scale = fp8 ? v_scale : 1.f;
     a.stages = stages;
-    a.smem_bytes = tc ? prefill_tc_smem_bytes() : 1024 + stages * stage_bytes + stages * 16 + 16;
+    a.smem_bytes = tc ? prefill_tc_smem_bytes()
+                      : fp8 ? 1024 + stages * stage_bytes + 1024 + raw_bytes
+                            : 1024 + stages * stage_bytes + stages * 16 + 32;
     a.tensor_cores = tc ? 1 : 0;
     a.tile_tokens = tc ? 128 / G : 16;
     const int64_t tiles = (static_cast<int64_t>(num_tokens) + a.tile_tokens - 1) / a.tile_tokens + num_seqs;
@@ -841,14 +861,41 @@ kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const vo
     a.grid_tiles = static_cast<int>(tiles);
     a.pdl = 1;
     a.device = dev;
-    CUtensorMap tk, tv;
-    const int rows = num_blocks * num_kv_heads * block_size;
-    const int box_rows = tc ? (block_size < 64 ? block_size : 64) : block_size;
-    if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, box_rows)) return st;
-    if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, box_rows)) return st;
+    CUtensorMap tk{}, tv{};
+    if (!fp8 && dtype != KV_F32) {  // E4M3 tiles come by bulk copies, f32 rows by plain loads
+        const int rows = num_blocks * num_kv_heads * block_size;
+        const int box_rows = tc ? (block_size < 64 ? block_size : 64) : block_size;
+        if (kv_status_t st = encode_cache_map(&tk, k_cache, dtype, rows, head_dim, box_rows)) return st;
+        if (kv_status_t st = encode_cache_map(&tv, v_cache, dtype, rows, head_dim, box_rows)) return st;
+    }
     cudaError_t e = launch_prefill(a, tk, tv, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return KV_OK;
+}
+
+kv_status_t paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                    const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                                    const int32_t* context_lens, int num_seqs, int num_tokens, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size, kv_dtype_t dtype,
+                                    float scale, void* out, kv_dtype_t out_dtype, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    if (dtype == KV_FP8_E4M3)
+        return fail(KV_ERR_INVALID_ARG, "paged_prefill_attention: an E4M3 cache goes to paged_prefill_attention_fp8");
+    return prefill_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, query_start, context_lens,
+                        num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, dtype, dtype, 1.f,
+                        1.f, scale, out, out_dtype, workspace, workspace_bytes, stream);
+}
+
+kv_status_t paged_prefill_attention_fp8(const void* q, kv_dtype_t q_dtype, const void* k_cache,
+                                        const void* v_cache, float k_scale, float v_scale, int num_blocks,
+                                        const int32_t* block_tables, int max_blocks, const int32_t* query_start,
+                                        const int32_t* context_lens, int num_seqs, int num_tokens,
+                                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                        float scale, void* out, kv_dtype_t out_dtype, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    return prefill_impl(q, k_cache, v_cache, num_blocks, block_tables, max_blocks, query_start, context_lens,
+                        num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, q_dtype,
+                        KV_FP8_E4M3, k_scale, v_scale, scale, out, out_dtype, workspace, workspace_bytes, stream);
 }
 
 kv_status_t kv_device_status(int device, void* stream, uint32_t* flags_out) {

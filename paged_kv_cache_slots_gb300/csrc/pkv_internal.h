@@ -117,7 +117,9 @@ struct PrefillArgs {
     uint32_t* status;
     int num_blocks, max_blocks, num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size;
     int dtype, out_dtype;
-    float scale_log2;
+    int kv_dtype;      // the cache: dtype, or kFP8 (E4M3 codes)
+    float scale_log2;  // scale * log2(e) (* k_scale for E4M3)
+    float v_scale;     // E4M3: a V code stands for v_scale * value (1 otherwise)
     int stages, smem_bytes, grid_tiles;
     int tile_tokens;   // new tokens per CTA (16, or 128 / G on the tcgen05 path)
     int tensor_cores;  // 1: the tcgen05 kernel (head_dim 128)

@@ -207,6 +207,8 @@ struct PrefillTile {
         }
     }
 
+    // vs: the V scale of an E4M3 cache (the stage holds the codes' values).
+    template <bool kScaled>
     __device__ __forceinline__ void finish(const PrefillArgs& a, int64_t tok0, int rows, int head) const {
         const int lane = threadIdx.x & 31;
         const int g = lane >> 2, c = lane & 3;
@@ -216,7 +218,11 @@ struct PrefillTile {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        const float i0 = 1.f / l0, i1 = 1.f / l1;
+        float i0 = 1.f / l0, i1 = 1.f / l1;
+        if constexpr (kScaled) {
+            i0 *= a.v_scale;
+            i1 *= a.v_scale;
+        }
         const int64_t o0 = ((tok0 + g) * a.num_q_heads + head) * D;
         const int64_t o1 = ((tok0 + g + 8) * a.num_q_heads + head) * D;
 #pragma unroll
@@ -234,12 +240,48 @@ struct PrefillTile {
     }
 };
 
+// E4M3 cache (kFP8, head_dim 128): the producer brings each block's codes
+// (a contiguous [bs][128] byte tile of K and one of V) into one of two raw
+// slots with a bulk copy, converts them exactly to q's type (every E4M3 value
+// is an f16 and a bf16) into the stage in the layout the tensor copies give
+// the other types (128-byte swizzle, rows of 64-element slices), and
+// completes the stage with a plain arrival.  The consumers are unchanged:
+// the K scale is folded into the score multiplier, the V scale into the
+// output.
+template <int DT>
+__device__ __forceinline__ void convert_e4m3_tile(const uint8_t* raw, uint8_t* stage, int bs) {
+    using T = typename Elem<DT>::T;
+    const int lane = threadIdx.x & 31;
+    const uint32_t slice_bytes = static_cast<uint32_t>(bs) * 128u;
+    for (int e = lane; e < bs * 16; e += 32) {  // (row, 8-code chunk) of a 128-code row
+        const int r = e >> 4, q = e & 15;        // q: the 8-dim chunk, dims 8q .. 8q + 7
+        const uint2 codes = *reinterpret_cast<const uint2*>(raw + r * 128 + q * 8);
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t word = k < 2 ? codes.x : codes.y;
+            const uint32_t h2 = e4m3x2_to_half2(static_cast<uint16_t>(word >> (16 * (k & 1))));
+            if constexpr (DT == kF16) {
+                w[k] = h2;
+            } else {
+                const __half2 hh = *reinterpret_cast<const __half2*>(&h2);
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__low2float(hh), __high2float(hh));
+                w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+        }
+        const int sl = q >> 3, c = q & 7;  // 64-dim slice and chunk within the 128-byte row
+        *reinterpret_cast<uint4*>(stage + sl * slice_bytes + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // G consumer warps (one per query head of the group) + the producer warp;
 // the register budget leaves room for several CTAs per SM.
-template <int DT, int D, int G>
+template <int DT, int D, int G, bool kFP8 = false>
 __global__ void __launch_bounds__(32 * (1 + G), G <= 4 ? 2 : 1) paged_prefill_kernel(const PrefillArgs a,
                                                                 const __grid_constant__ CUtensorMap tmk,
                                                                 const __grid_constant__ CUtensorMap tmv) {
+    static_assert(!kFP8 || D == 128, "E4M3 rows of 128 codes");
     extern __shared__ uint8_t smem_raw[];
     pdl_allow_next();
     pdl_wait();
@@ -262,19 +304,85 @@ __global__ void __launch_bounds__(32 * (1 + G), G <= 4 ? 2 : 1) paged_prefill_ke
     const int stage_bytes = 2 * half;
     uint64_t* full = reinterpret_cast<uint64_t*>(base + a.stages * stage_bytes);
     uint64_t* empty = full + a.stages;
-    volatile int* abort = reinterpret_cast<volatile int*>(empty + a.stages);
+    uint64_t* raw_full = empty + a.stages;  // kFP8: the two raw slots' copies
+    volatile int* abort = reinterpret_cast<volatile int*>(raw_full + 2);
+    uint8_t* raw = base + a.stages * stage_bytes + 1024;  // kFP8: 2 slots x (K, V) x bs x 128 codes
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int st = 0; st < a.stages; ++st) {
             mbar_init(&full[st], 1);
             mbar_init(&empty[st], G);
         }
+        mbar_init(&raw_full[0], 1);
+        mbar_init(&raw_full[1], 1);
         *abort = 0;
         fence_barrier_init();
-        prefetch_tensor_map(&tmk);
-        prefetch_tensor_map(&tmv);
+        if constexpr (!kFP8) {
+            prefetch_tensor_map(&tmk);
+            prefetch_tensor_map(&tmv);
+        }
     }
     __syncthreads();
+    if (kFP8 && warp == 0) {
+        // ---- producer (E4M3): bulk copies into the raw slots, conversion into the stages
+        const uint64_t policy = policy_evict_last();
+        const uint32_t tile = static_cast<uint32_t>(bs) * 128u;  // one (block, head) tile of codes
+        auto block_of = [&](int j) {
+            int blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + j];
+            if (blk < 0 || blk >= a.num_blocks) {
+                raise_flag(a.status, kFlagBadBlock);
+                blk = 0;
+            }
+            return blk;
+        };
+        auto fetch = [&](int j) {  // block j's K and V codes into raw slot j % 2 (lane 0)
+            uint8_t* dst = raw + (j & 1) * 2 * tile;
+            fence_proxy_async_smem();  // the slot's last reads (generic) before the copy (async)
+            const int64_t off = (static_cast<int64_t>(block_of(j)) * a.num_kv_heads + h) * tile;
+            mbar_arrive_expect_tx(&raw_full[j & 1], 2 * tile);
+            bulk_load(dst, static_cast<const uint8_t*>(a.k_cache) + off, tile, &raw_full[j & 1], policy);
+            bulk_load(dst + tile, static_cast<const uint8_t*>(a.v_cache) + off, tile, &raw_full[j & 1], policy);
+        };
+        int fetched = 0;  // raw copies issued (lane 0)
+        if (lane == 0 && nblocks > 0) {
+            fetch(0);
+            fetched = 1;
+        }
+        for (int j = 0; j < nblocks; ++j) {
+            const int stage = j % a.stages;
+            int good = 1;
+            if (lane == 0) {
+                if (j + 1 < nblocks) {  // the next block's codes, into the slot block j - 1 left
+                    fetch(j + 1);
+                    ++fetched;
+                }
+                if (j >= a.stages)
+                    good = mbar_wait_bounded(&empty[stage], ((j / a.stages) - 1) & 1, abort, a.status);
+                if (good) good = mbar_wait_bounded(&raw_full[j & 1], (j >> 1) & 1, abort, a.status);
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) break;
+            uint8_t* kd = base + stage * stage_bytes;
+            convert_e4m3_tile<DT>(raw + (j & 1) * 2 * tile, kd, bs);
+            convert_e4m3_tile<DT>(raw + (j & 1) * 2 * tile + tile, kd + half, bs);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[stage]);
+        }
+        // Every raw copy issued must land before the CTA exits (bounded).
+        if (lane == 0) {
+            for (int sl = 0; sl < 2 && sl < fetched; ++sl) {
+                const int lastj = sl + ((fetched - 1 - sl) / 2) * 2;
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&raw_full[sl], (lastj >> 1) & 1)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        raise_flag(a.status, kFlagTimeout);
+                        break;
+                    }
+                }
+            }
+        }
+        return;
+    }
     if (warp == 0) {
         // ---- producer: K and V tiles of blocks 0 .. nblocks-1 of head h
         const uint64_t policy = policy_evict_last();
@@ -369,14 +477,14 @@ __global__ void __launch_bounds__(32 * (1 + G), G <= 4 ? 2 : 1) paged_prefill_ke
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
     }
-    if (!*abort) t.finish(a, tok0, rows, head);
+    if (!*abort) t.template finish<kFP8>(a, tok0, rows, head);
 }
 
-template <int DT, int D, int G>
+template <int DT, int D, int G, bool kFP8>
 cudaError_t launch_prefill_g(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t stream) {
     static std::atomic<int> configured[64];
-    auto kern = paged_prefill_kernel<DT, D, G>;
+    auto kern = paged_prefill_kernel<DT, D, G, kFP8>;
     const bool cacheable = a.device >= 0 && a.device < 64;
     if (!cacheable || configured[a.device].load() < a.smem_bytes) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, a.smem_bytes);
@@ -387,15 +495,89 @@ cudaError_t launch_prefill_g(const PrefillArgs& a, const CUtensorMap& tmk, const
                          static_cast<size_t>(a.smem_bytes), stream, a.pdl != 0, a, tmk, tmv);
 }
 
-template <int DT, int D>
+template <int DT, int D, bool kFP8 = false>
 cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t stream) {
     switch (a.num_q_heads / a.num_kv_heads) {
-        case 1: return launch_prefill_g<DT, D, 1>(a, tmk, tmv, stream);
-        case 2: return launch_prefill_g<DT, D, 2>(a, tmk, tmv, stream);
-        case 4: return launch_prefill_g<DT, D, 4>(a, tmk, tmv, stream);
-        case 8: return launch_prefill_g<DT, D, 8>(a, tmk, tmv, stream);
+        case 1: return launch_prefill_g<DT, D, 1, kFP8>(a, tmk, tmv, stream);
+        case 2: return launch_prefill_g<DT, D, 2, kFP8>(a, tmk, tmv, stream);
+        case 4: return launch_prefill_g<DT, D, 4, kFP8>(a, tmk, tmv, stream);
+        case 8: return launch_prefill_g<DT, D, 8, kFP8>(a, tmk, tmv, stream);
     }
+    return cudaErrorInvalidValue;
+}
+
+// f32 q and cache: one warp per (new token, query head), the token's causal
+// prefix one key at a time on the CUDA cores (lane l holds dims VD*l ..
+// VD*l + VD - 1; the dot product reduced across the warp), online softmax in
+// base 2.  A sequence whose chunk is longer than its context, or whose context
+// exceeds its table, writes nothing (the plan kernel flags it).
+template <int D>
+__global__ void __launch_bounds__(256) paged_prefill_f32_kernel(const PrefillArgs a) {
+    constexpr int VD = D / 32;
+    pdl_allow_next();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= static_cast<int64_t>(a.num_tokens) * a.num_q_heads) return;
+    const int64_t tok = row / a.num_q_heads;
+    const int g = static_cast<int>(row - tok * a.num_q_heads);
+    const int h = g / (a.num_q_heads / a.num_kv_heads);
+    int lo = 0, hi = a.num_seqs;  // the sequence of the token: largest s with query_start[s] <= tok
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a.query_start[mid] <= tok) lo = mid; else hi = mid;
+    }
+    const int s = lo;
+    const int n = a.query_start[s + 1] - a.query_start[s];
+    const int ctx = a.context_lens[s];
+    if (n <= 0 || n > ctx || ctx > a.max_blocks * a.block_size) return;
+    const int pos = ctx - n + static_cast<int>(tok - a.query_start[s]);
+    const float* qrow = static_cast<const float*>(a.q) + row * D + VD * lane;
+    float q[VD], o[VD];
+#pragma unroll
+    for (int i = 0; i < VD; ++i) {
+        q[i] = qrow[i] * a.scale_log2;
+        o[i] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const float* kc = static_cast<const float*>(a.k_cache);
+    const float* vc = static_cast<const float*>(a.v_cache);
+    for (int t = 0; t <= pos; ++t) {
+        int blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + t / a.block_size];
+        if (blk < 0 || blk >= a.num_blocks) {
+            if (lane == 0) raise_flag(a.status, kFlagBadBlock);
+            blk = 0;
+        }
+        const int64_t r = (static_cast<int64_t>(blk) * a.num_kv_heads + h) * a.block_size + t % a.block_size;
+        const float* k = kc + r * D + VD * lane;
+        const float* v = vc + r * D + VD * lane;
+        float x = 0.f;
+#pragma unroll
+        for (int i = 0; i < VD; ++i) x = fmaf(q[i], __ldg(k + i), x);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+        const float mn = fmaxf(m, x);
+        const float al = fast_exp2(m - mn);  // 0 while m is -inf
+        const float p = fast_exp2(x - mn);
+        l = fmaf(l, al, p);
+#pragma unroll
+        for (int i = 0; i < VD; ++i) o[i] = fmaf(o[i], al, p * __ldg(v + i));
+        m = mn;
+    }
+    const float inv = 1.f / l;
+    float* out = static_cast<float*>(a.out) + row * D + VD * lane;
+#pragma unroll
+    for (int i = 0; i < VD; ++i) out[i] = o[i] * inv;
+}
+
+cudaError_t launch_prefill_f32(const PrefillArgs& a, cudaStream_t stream) {
+    const int64_t warps = static_cast<int64_t>(a.num_tokens) * a.num_q_heads;
+    const int blocks = static_cast<int>((warps + 7) / 8);
+    if (a.head_dim == 64) return launch_kernel(paged_prefill_f32_kernel<64>, dim3(blocks), dim3(256), 0, stream,
+                                               a.pdl != 0, a);
+    if (a.head_dim == 128) return launch_kernel(paged_prefill_f32_kernel<128>, dim3(blocks), dim3(256), 0, stream,
+                                                a.pdl != 0, a);
     return cudaErrorInvalidValue;
 }
 
@@ -406,6 +588,13 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& tmk, const C
     if (a.num_seqs == 0 || a.num_tokens == 0) return cudaSuccess;
     cudaError_t e = launch_kernel(prefill_plan_kernel, dim3(1), dim3(1024), 0, stream, a.pdl != 0, a);
     if (e != cudaSuccess) return e;
+    if (a.kv_dtype == kFP8) {
+        if (a.head_dim != 128) return cudaErrorInvalidValue;
+        if (a.dtype == kF16) return launch_prefill_t<kF16, 128, true>(a, tmk, tmv, stream);
+        if (a.dtype == kBF16) return launch_prefill_t<kBF16, 128, true>(a, tmk, tmv, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (a.dtype == kF32) return launch_prefill_f32(a, stream);
     if (a.tensor_cores) return launch_prefill_tc(a, tmk, tmv, stream);
     if (a.dtype == kF16) {
         if (a.head_dim == 64) return launch_prefill_t<kF16, 64>(a, tmk, tmv, stream);

@@ -169,8 +169,9 @@ def test_bad_lengths_flagged_and_skipped():
     assert flags & pkv.FLAG_BAD_CONTEXT and st != 0
     assert torch.all(out[4:] == 7.0)  # the bad sequence's rows are not written
     assert torch.isfinite(out[:4]).all()
-    with pytest.raises(pkv.KVError):
-        pkv.paged_prefill_attention(q.float(), k_pre.float(), v_pre.float(), tables, qs, ctx, 0.1)
+    with pytest.raises(pkv.KVError):  # f16 needs blocks of a multiple of 16 tokens
+        pkv.paged_prefill_attention(q, k_pre.view(-1, 2, 8, 64).contiguous(), v_pre.view(-1, 2, 8, 64).contiguous(),
+                                    tables, qs, ctx, 0.1)
 
 
 def test_chunked_prefill_b32_full_size_sampled():
@@ -222,3 +223,93 @@ def test_chunked_prefill_b32_full_size_sampled():
                                   np.array([pos + 1], np.int32), spec.attn_scale)
         check_output(out[t:t + 1], ref, f"chunked_prefill_b32 sequence {s} token {i} (position {pos})")
 
+
+# ------------------------------------------------------------ f32 and E4M3
+F32_CTX = (1, 15, 16, 17, 40, 100, 33)
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("block_size", [8, 16, 48])
+def test_f32_multi_token_queries(head_dim, group, block_size):
+    """f32 q and cache (the CUDA-core kernel, any block size): every output."""
+    spec = small_spec(f"prefill_f32_{head_dim}_{group}_{block_size}", num_q_heads=2 * group, num_kv_heads=2,
+                      head_dim=head_dim, block_size=block_size, dtype="f32", seed=200 + head_dim + group + block_size,
+                      ctx=F32_CTX)
+    nq = new_token_counts(F32_CTX, seed=group, max_chunk=40)
+    nq[3] = F32_CTX[3]  # one whole prompt
+    _step(spec, nq)
+
+
+def _step_fp8(spec, nq, out_dtype=torch.float32, scale=None):
+    """The multi-token step over an E4M3 cache: varlen slots, the quantizing
+    append of every new token (codes bit-exact) and the causal attention over
+    the codes times the scales, against the oracle."""
+    scale = spec.attn_scale if scale is None else scale
+    ks, vs = spec.kv_scales
+    pl = make_placement(spec)
+    ctx = pl.context_lens
+    nq = np.asarray(nq, np.int32)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    T = int(qs[-1])
+    k_pre, v_pre = pool_layer_values(spec, pl.num_blocks, 0, "cpu")
+    q, kn, vn = step_token_values(spec, T, 0, "cpu")
+    o_slots = oracle.slot_mapping_varlen(pl.block_tables, qs, ctx, spec.block_size)
+    k_post, v_post = oracle.append_e4m3(k_pre, v_pre, kn, vn, o_slots, ks, vs)
+    ref = oracle.paged_prefill(q, k_post, v_post, pl.block_tables, qs, ctx, scale, k_scale=ks, v_scale=vs)
+    pool = pkv.KVPool(1, pl.num_blocks, spec.block_size, spec.num_kv_heads, spec.head_dim, torch.float8_e4m3fn)
+    kc, vc = pool.layer(0)
+    kc.view(torch.uint8).copy_(k_pre.view(torch.uint8))
+    vc.view(torch.uint8).copy_(v_pre.view(torch.uint8))
+    tables = torch.from_numpy(pl.block_tables).cuda()
+    ctx_d = torch.from_numpy(ctx).cuda()
+    qs_d = torch.from_numpy(qs).cuda()
+    slots = pkv.slot_mapping_varlen(tables, qs_d, ctx_d, spec.block_size, pl.num_blocks, num_tokens=T)
+    pool.append(0, kn.cuda(), vn.cuda(), slots, k_scale=ks, v_scale=vs)
+    out = torch.full((T, spec.num_q_heads, spec.head_dim), float("nan"), dtype=out_dtype, device="cuda")
+    pkv.paged_prefill_attention(q.cuda(), kc, vc, tables, qs_d, ctx_d, scale, out=out, out_dtype=out_dtype,
+                                k_scale=ks, v_scale=vs)
+    assert pkv.device_status() == (0, 0)
+    assert np.array_equal(slots.cpu().numpy(), o_slots), "varlen slot mapping"
+    assert torch.equal(kc.view(torch.uint8).cpu(), k_post.view(torch.uint8)), "K codes after the append"
+    assert torch.equal(vc.view(torch.uint8).cpu(), v_post.view(torch.uint8)), "V codes after the append"
+    if out_dtype != torch.float32:
+        out32 = torch.full_like(out, float("nan"), dtype=torch.float32)
+        pkv.paged_prefill_attention(q.cuda(), kc, vc, tables, qs_d, ctx_d, scale, out=out32,
+                                    out_dtype=torch.float32, k_scale=ks, v_scale=vs)
+        check_output(out32, ref, f"{spec.name} E4M3 prefill fp32")
+        check_cast(out, out32, f"{spec.name} E4M3 prefill")
+    return check_output(out, ref, f"{spec.name} E4M3 prefill {out_dtype}")
+
+
+FP8_SCALES = (1.0 / 56.0, 1.0 / 44.0)
+FP8_CTX = (1, 15, 16, 17, 33, 64, 100, 257, 40)
+
+
+@pytest.mark.parametrize("qdtype", ["f16", "bf16"])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_fp8_multi_token_queries(qdtype, group):
+    spec = small_spec(f"prefill_fp8_{qdtype}_{group}", num_q_heads=2 * group, num_kv_heads=2, head_dim=128,
+                      block_size=16, dtype=qdtype, seed=300 + group, ctx=FP8_CTX, kv_dtype="e4m3",
+                      kv_scales=FP8_SCALES)
+    nq = new_token_counts(FP8_CTX, seed=group, max_chunk=70)
+    nq[-1] = FP8_CTX[-1]  # one whole prompt
+    _step_fp8(spec, nq)
+
+
+@pytest.mark.parametrize("block_size", [32, 64, 128])
+def test_fp8_multi_token_block_sizes_and_output_type(block_size):
+    ctx = (1, block_size - 1, block_size + 1, 3 * block_size + 5, 200)
+    spec = small_spec(f"prefill_fp8_bs{block_size}", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                      block_size=block_size, dtype="bf16", seed=310 + block_size, ctx=ctx, kv_dtype="e4m3",
+                      kv_scales=(0.0173, 0.0219))
+    _step_fp8(spec, new_token_counts(ctx, seed=5, max_chunk=150), out_dtype=torch.bfloat16)
+
+
+def test_fp8_long_chunk_and_negative_scale():
+    # A 700-token chunk after 2,000 cached tokens next to decodes, the 8B
+    # head shape; and a negative scale over the same cache.
+    spec = small_spec("prefill_fp8_long", num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                      dtype="bf16", seed=321, ctx=(2700, 40, 1, 900), kv_dtype="e4m3", kv_scales=FP8_SCALES)
+    _step_fp8(spec, [700, 1, 1, 1])
+    _step_fp8(spec, [700, 1, 1, 1], scale=-0.05)
